@@ -1,0 +1,421 @@
+"""Benchmark of MLA decode over a paged latent KV cache on GB300.
+
+One step = the whole hot path once: the split-KV schedule (mla_get_metadata),
+the split-KV decode kernel and the log-sum-exp combine, over one batch of the
+workload.  Default workload: b=128, s_q=1, h_q=128, h_kv=1, d=576, dv=512,
+64-token pages, every sequence 4096 tokens, 576-element entries, pages in
+order (the shape of FlashMLA's benchmark in the PAI tutorial, section 4).
+
+Metric (the benchmark's own formula, compare_a in that section):
+  bytes = (sum(seqlens)*h_kv*576 + b*s_q*h_q*576 + b*s_q*h_q*512) * 2
+  flops = 2 * s_q * sum(seqlens) * h_q * (576 + 512)
+  GB/s  = bytes / 1e6 / ms        TFLOPS = flops / 1e9 / ms
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (whole sequences, all heads).
+
+Prints one JSON line.  Run with no flags for N=1; under torchrun each rank runs
+its own replica of the workload (no data-path collective) and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mla_decode_attention_03_gb300 import workloads as W  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20
+
+
+def metric_bytes_flops(w) -> tuple[int, int]:
+    S = int(w.cache_seqlens.sum())
+    b, s_q, h_q = w.b, w.s_q, w.h_q
+    nbytes = (S * w.h_kv * 576 + b * s_q * h_q * 576 + b * s_q * h_q * 512) * 2
+    flops = 2 * s_q * S * h_q * (576 + 512)
+    return nbytes, flops
+
+
+def describe(w) -> str:
+    sl = w.cache_seqlens.numpy()
+    lens = f"L={int(sl[0])} for all" if (sl == sl[0]).all() else \
+        f"L in [{int(sl.min())},{int(sl.max())}] sum {int(sl.sum())}"
+    return (f"{w.name}: MLA decode b={w.b} s_q={w.s_q} h_q={w.h_q} h_kv={w.h_kv} d=576 dv=512 "
+            f"page=64 {lens} entry stride {w.stride} causal={int(w.causal)}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[2:6]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    from mla_decode_attention_03_gb300 import ops
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = W.named(args.workload, stride=args.stride)
+    nbytes, flops = metric_bytes_flops(w)
+    q = w.q.to(dev)
+    kc_alloc = w.kcache_alloc.to(dev)
+    kc = kc_alloc[..., :576]
+    bt = w.block_table.to(dev)
+    sl = w.cache_seqlens.to(dev)
+    parts = ops.num_parts(w.s_q, w.h_q, w.h_kv, dev)
+    dec = ops.MLADecoder(w.b, w.s_q, w.h_q, w.h_kv, device=dev, parts=parts)
+    out = torch.empty((w.b, w.s_q, w.h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.b, w.h_q, w.s_q), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        meta, nsplit = ops.get_mla_metadata(sl, parts, dec.status)
+        if ev is not None:
+            ev[1].record(stream)
+        ops.mla_decode_with_kvcache(q, kc, bt, sl, meta, nsplit, w.softmax_scale, w.causal, out=out,
+                                    lse=lse, workspace=dec.workspace, status=dec.status, combine=False)
+        if ev is not None:
+            ev[2].record(stream)
+        ops.combine_splits(nsplit, dec.workspace, parts, out, lse)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    ops.check_status(dec.status)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)  # L2 flush: a 512 MB write between steps, outside the events
+            step(evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    ops.check_status(dec.status)
+    t_meta = [e[0].elapsed_time(e[1]) for e in evs]
+    t_dec = [e[1].elapsed_time(e[2]) for e in evs]
+    t_comb = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    ms_step = max_over_ranks(float(np.mean(t_step)), world)
+    ms_dec = float(np.mean(t_dec))
+
+    # end to end through the public API: pinned host q / block_table / seqlens in,
+    # out / lse back, the cache resident in HBM
+    e2e = run_e2e(args, w, dev, kc, parts, dec, flush, nbytes)
+
+    hbm_peak, tf_peak, peak_src = peaks()
+    achieved = nbytes / 1e9 / (ms_dec / 1e3)
+    value = world * nbytes / 1e6 / ms_step
+    line = {
+        "metric": "MLA decode achieved GB/s (pages' bandwidth formula), whole step",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 q and cache (numpy PCG64), no weights",
+        "config": {
+            "workload": describe(w),
+            "b": w.b, "s_q": w.s_q, "h_q": w.h_q, "h_kv": w.h_kv, "stride": w.stride,
+            "sum_seqlens": int(w.cache_seqlens.sum()),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "num_parts": parts,
+            "l2": "flushed between steps by a 512 MB write outside the timed events",
+            "step": "metadata + split-KV decode + combine",
+            "bytes_per_step": nbytes, "flops_per_step": flops,
+        },
+        "tflops": round(world * flops / 1e9 / ms_step, 1),
+        "breakdown_us": {"metadata": round(1e3 * float(np.mean(t_meta)), 2),
+                         "decode": round(1e3 * ms_dec, 2),
+                         "combine": round(1e3 * float(np.mean(t_comb)), 2),
+                         "decode_median": round(1e3 * float(np.median(t_dec)), 2)},
+        "wall_s_timed_loop": round(wall, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "kernel": "mla_decode_kernel", "peak_source": peak_src,
+                     "tensor_tflops_achieved": round(flops / 1e9 / ms_dec, 1),
+                     "tensor_frac": round(flops / 1e9 / ms_dec / tf_peak, 4)},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, dev, kc, parts, dec, flush, nbytes):
+    from mla_decode_attention_03_gb300 import ops
+
+    q_h = w.q.pin_memory()
+    bt_h = w.block_table.pin_memory()
+    sl_h = w.cache_seqlens.pin_memory()
+    out_h = torch.empty((w.b, w.s_q, w.h_q, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((w.b, w.h_q, w.s_q), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(q_h, device=dev)
+    bt_d = torch.empty_like(bt_h, device=dev)
+    sl_d = torch.empty_like(sl_h, device=dev)
+    out_d = torch.empty_like(out_h, device=dev)
+    lse_d = torch.empty_like(lse_h, device=dev)
+    stream = torch.cuda.current_stream()
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        meta, nsplit = ops.get_mla_metadata(sl_d, parts, dec.status)
+        ops.mla_decode_with_kvcache(q_d, kc, bt_d, sl_d, meta, nsplit, w.softmax_scale, w.causal,
+                                    out=out_d, lse=lse_d, workspace=dec.workspace, status=dec.status)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 200))
+    times = []
+    for k in range(n):
+        flush.fill_(k & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+    return {"value": round(nbytes / 1e6 / ms, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "pinned host q/block_table/seqlens in, out/lse out; the KV cache stays resident"}
+
+
+# ----------------------------------------------------------- CPU baseline
+def sample_rows(w, n_rows: int, offset: int = 0) -> np.ndarray:
+    """A bounded sample of the workload's output rows: whole sequences (all
+    query positions and heads) taken in order from `offset`, or a leading run
+    of one sequence's rows when n_rows is below one sequence."""
+    per_seq = w.s_q * w.h_q
+    rows = []
+    i = offset % w.b
+    while len(rows) < n_rows:
+        take = min(per_seq, n_rows - len(rows))
+        for r in range(take):
+            rows.append((i, r // w.h_q, r % w.h_q))
+        i = (i + 1) % w.b
+    return np.asarray(rows, dtype=np.int32)
+
+
+def sample_bytes(w, rows) -> float:
+    """The metric's bytes attributable to a row sample: each sequence's cache
+    bytes in proportion to the share of its rows sampled, plus the q and out
+    bytes of the sampled rows (for whole sequences this is the formula itself)."""
+    per_seq = w.s_q * w.h_q
+    seqs, counts = np.unique(rows[:, 0], return_counts=True)
+    L = w.cache_seqlens.numpy()[seqs].astype(np.float64)
+    cache = float((L * w.h_kv * 576 * 2 * counts / per_seq).sum())
+    return cache + len(rows) * (576 + 512) * 2
+
+
+def time_oracle(w, rows, bits):
+    import oracle
+    qb, kb = bits
+    t0 = time.perf_counter()
+    oracle.decode_rows(qb, kb, w.block_table.numpy(), w.cache_seqlens.numpy(), rows,
+                       softmax_scale=w.softmax_scale, causal=w.causal)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, target_s: float = 10.0):
+    """The oracle, as it stands, on the host cores: a probe of 2 sequences sets
+    the sample size to about `target_s` seconds of work (capped at the whole batch)."""
+    import oracle
+    bits = w.numpy_bits()
+    per_seq = w.s_q * w.h_q
+    probe = sample_rows(w, 2 * per_seq)
+    dt = time_oracle(w, probe, bits)
+    n_seqs = int(max(2, min(w.b, round(2 * target_s / max(dt, 1e-3)))))
+    rows = sample_rows(w, n_seqs * per_seq)
+    dt = time_oracle(w, rows, bits)
+    nbytes = sample_bytes(w, rows)
+    return {"value": round(nbytes / 1e6 / (dt * 1e3), 4), "unit": "GB/s",
+            "cores": oracle.host_threads(), "kind": "oracle",
+            "sample": f"{n_seqs} of {w.b} sequences, every query position and head "
+                      f"({len(rows)} rows), {dt:.1f} s of fp64 C on the host cores"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = W.named(args.workload, stride=args.stride)
+    bits = w.numpy_bits()
+    # about two minutes of oracle work in total, whatever --steps is
+    n_rows = int(max(16, min(16 * w.s_q * w.h_q, 150000 // max(1, args.steps + args.warmup))))
+    for k in range(args.warmup):
+        time_oracle(w, sample_rows(w, n_rows, k), bits)
+    times, total_bytes = [], 0
+    for k in range(args.steps):
+        rows = sample_rows(w, n_rows, args.warmup + k)
+        times.append(time_oracle(w, rows, bits))
+        total_bytes += sample_bytes(w, rows)
+    ms = 1e3 * sum(times) / len(times)
+    value = total_bytes / 1e6 / (1e3 * sum(times))
+    sample = f"{n_rows} output rows per step (whole sequences in order when >= {w.s_q * w.h_q})"
+    line = {
+        "impl": "reference",
+        "metric": "MLA decode achieved GB/s (pages' bandwidth formula), whole step",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "sample_per_step": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.host_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bench", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--stride", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

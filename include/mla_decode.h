@@ -1,0 +1,169 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library
+ * (libmla_decode.so).
+ *
+ * The operation is Multi-head Latent Attention decode over a paged latent KV
+ * cache: the computation of FlashMLA's flash_mla_with_kvcache and
+ * get_mla_metadata, as the PAI tutorial "云上玩转DeepSeek系列之五" calls them
+ * from vLLM (section 2, FlashMLAImpl / FlashMLAMetadataBuilder) and
+ * benchmarks them (section 4, compare_a: q[b, s_q, h_q, d],
+ * blocked_k[num_blocks, 64, h_kv, d], block_table, cache_seqlens, dv, causal,
+ * returning out and lse).  For sequence i, query position j and head h, with
+ * g = h / (h_q / h_kv):
+ *
+ *   visible t:  t < L_i, and with causal also t <= L_i - s_q + j
+ *   K_t = kcache[block_table[i][t/64]][t%64][g][0:576],  V_t = K_t[0:512]
+ *   out[i,j,h,:] = sum_t softmax_t(softmax_scale * <q[i,j,h,:], K_t>) V_t
+ *   lse[i,h,j]   = ln sum_t exp(softmax_scale * <q[i,j,h,:], K_t>)
+ *
+ * A row with no visible token gets out = 0 and lse = -inf.  The split of the
+ * KV length across SMs and the merge of the pieces by their log-sum-exps is
+ * Flash-Decoding's (Hacker News thread on the FlashMLA release).  A cache
+ * entry may be padded: `stride` is the number of elements from one entry to
+ * the next, 576 or the 256-byte aligned 640 of vLLM PR #12676 ("Mem align KV
+ * caches for CUDA devices"); the padding is never read.
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers on the current CUDA device, owned
+ *    by the caller.  The library allocates nothing and never synchronises; the
+ *    calls only enqueue kernels on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and may be captured in a CUDA graph.
+ *  - bf16 arrays are passed as void* holding IEEE bfloat16 values.
+ *  - Arguments that the host can check are checked before anything is
+ *    enqueued; a failed check returns a negative mla_status_t and enqueues
+ *    nothing.
+ *  - Problems only the device can see (a page id outside [0, num_blocks), a
+ *    negative sequence length, an internal wait that timed out) are written to
+ *    the caller's int32 `status` word in device memory.  The library never
+ *    clears it: set it to 0 before the calls and read it after synchronising.
+ *    A kernel that reports an error still exits normally; its outputs are then
+ *    unspecified.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mla_status_t;
+enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,  /* a shape or size outside what the call accepts   */
+  MLA_ERR_UNSUPPORTED = -2,  /* legal in principle, not built here (e.g. d != 576) */
+  MLA_ERR_ALIGNMENT = -3,    /* a pointer or stride not 16-byte aligned          */
+  MLA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed                */
+  MLA_ERR_BAD_BLOCK_ID = -5, /* device: block_table entry outside the cache      */
+  MLA_ERR_TIMEOUT = -6,      /* device: a pipeline wait gave up                  */
+  MLA_ERR_BAD_SEQLEN = -7    /* device: cache_seqlens entry < 0                  */
+};
+
+typedef struct CUstream_st *mla_stream_t; /* the same type as cudaStream_t */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *mla_status_string(mla_status_t status);
+
+/*
+ * Recommended number of scheduler parts for `device`: how many 2-CTA decode
+ * clusters fit on the GPU at once, divided among the (row tile, KV head)
+ * grid dimensions of this shape.  Returns a count >= 1, or a negative
+ * mla_status_t.  The first call per device queries occupancy; later calls are
+ * cheap.
+ */
+int mla_num_parts(int s_q, int h_q, int h_kv, int device);
+
+/* Size of the metadata array in int32 elements: num_parts x 8. */
+size_t mla_metadata_ints(int num_parts);
+
+/*
+ * Bytes of scratch the decode call needs for split partial results:
+ * (b + num_parts) x s_q x h_q x (512 + 1) fp32 values, plus alignment.
+ */
+size_t mla_workspace_bytes(int b, int s_q, int h_q, int num_parts);
+
+/*
+ * Split-KV schedule (the role of FlashMLA's get_mla_metadata, called once per
+ * decode step and shared by every layer).  Cuts the (sequence, page) order of
+ * the batch into num_parts contiguous, cost-balanced parts; each part becomes
+ * one 2-CTA cluster of the decode kernel.
+ *   cache_seqlens  int32[b]            tokens per sequence (device)
+ *   b              1 .. 16384
+ *   num_parts      >= 1 (normally mla_num_parts())
+ *   metadata       int32[num_parts*8]  out: per part {first seq, first page,
+ *                                       last seq, end page, first split index, 0,0,0}
+ *   num_splits     int32[b+1]          out: exclusive prefix sum of the number
+ *                                       of pieces each sequence is cut into
+ *   status         int32[1]            device error word (see conventions)
+ * One single-block kernel on `stream`; no host synchronisation.
+ */
+mla_status_t mla_get_metadata(const int32_t *cache_seqlens, int b, int num_parts,
+                              int32_t *metadata, int32_t *num_splits, int32_t *status,
+                              mla_stream_t stream);
+
+/*
+ * MLA decode over the paged latent cache (the role of flash_mla_with_kvcache).
+ *   q             bf16[b, s_q, h_q, d], contiguous, 16-byte aligned
+ *   d             must be 576 (512 latent + 64 rope)
+ *   kcache        bf16, entry (page, slot, g) at
+ *                 kcache + ((page*block_size + slot)*h_kv + g)*stride; 16-byte aligned
+ *   num_blocks    pages in the cache (num_blocks*64 < 2^31)
+ *   block_size    must be 64
+ *   h_kv          KV heads; h_q % h_kv == 0 and h_q/h_kv <= 128
+ *   stride        elements per entry, >= 576 and a multiple of 8 (576 or 640)
+ *   block_table   int32[b, max_blocks_per_seq]; only the first ceil(L_i/64)
+ *                 entries of row i are read
+ *   cache_seqlens int32[b], 0 <= L_i <= max_blocks_per_seq*64
+ *   dv            must be 512
+ *   metadata, num_parts, num_splits: from mla_get_metadata on the same
+ *                 cache_seqlens (and the same num_parts)
+ *   softmax_scale finite (FlashMLA's benchmark uses d**-0.5)
+ *   causal        0 or 1; with 1, query j sees tokens t <= L_i - s_q + j
+ *   out           bf16[b, s_q, h_q, 512], 16-byte aligned (written)
+ *   lse           fp32[b, h_q, s_q], natural log (written)
+ *   workspace     >= mla_workspace_bytes(b, s_q, h_q, num_parts) bytes,
+ *                 16-byte aligned, contents need not be initialised
+ *   status        int32[1] device error word
+ * Enqueues the decode kernel and the combine kernel on `stream`.
+ */
+mla_status_t mla_decode_with_kvcache(const void *q, int b, int s_q, int h_q, int d,
+                                     const void *kcache, int64_t num_blocks, int block_size,
+                                     int h_kv, int stride, const int32_t *block_table,
+                                     int max_blocks_per_seq, const int32_t *cache_seqlens,
+                                     int dv, const int32_t *metadata, int num_parts,
+                                     const int32_t *num_splits, float softmax_scale, int causal,
+                                     void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t *status,
+                                     mla_stream_t stream);
+
+/*
+ * The two halves of mla_decode_with_kvcache, for callers that time or
+ * schedule them separately.  mla_decode_splitkv takes the same arguments and
+ * runs only the decode kernel: sequences cut into one piece get their out and
+ * lse written directly; the pieces of the others go to `workspace` as
+ * normalised fp32 partial outputs and natural-log partial lse.
+ * mla_combine_splits then merges those pieces by their log-sum-exps (the
+ * Flash-Decoding merge) into out and lse, and writes out = 0, lse = -inf for
+ * sequences of length 0.  It must run after mla_decode_splitkv on the same
+ * workspace, b, s_q, h_q and num_parts; ordering on one stream suffices.
+ */
+mla_status_t mla_decode_splitkv(const void *q, int b, int s_q, int h_q, int d,
+                                const void *kcache, int64_t num_blocks, int block_size,
+                                int h_kv, int stride, const int32_t *block_table,
+                                int max_blocks_per_seq, const int32_t *cache_seqlens, int dv,
+                                const int32_t *metadata, int num_parts,
+                                const int32_t *num_splits, float softmax_scale, int causal,
+                                void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                int32_t *status, mla_stream_t stream);
+
+mla_status_t mla_combine_splits(const int32_t *num_splits, int b, int s_q, int h_q,
+                                const void *workspace, int num_parts, void *out, float *lse,
+                                mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

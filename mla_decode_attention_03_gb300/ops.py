@@ -1,0 +1,197 @@
+"""Python binding of libmla_decode.so (include/mla_decode.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  Tensors must already live on the current CUDA
+device; outputs, metadata and scratch are torch allocations owned by the
+caller.  There is no CPU path: if the library is missing or no GPU is present
+the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libmla_decode.so"
+D_QK, D_V, BLOCK_SIZE = 576, 512, 64
+
+_lib = None
+
+
+class MLAError(RuntimeError):
+    pass
+
+
+def load_library():
+    """Loads libmla_decode.so (built by mla_decode_attention_03_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not LIB_PATH.exists():
+        raise MLAError(f"{LIB_PATH} is missing: build it with "
+                       "`python -m mla_decode_attention_03_gb300.build` (needs nvcc for sm_103a)")
+    lib = ctypes.CDLL(str(LIB_PATH))
+    P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_status_string.argtypes = [ctypes.c_int32]
+    lib.mla_num_parts.restype = I
+    lib.mla_num_parts.argtypes = [I, I, I, I]
+    lib.mla_metadata_ints.restype = SZ
+    lib.mla_metadata_ints.argtypes = [I]
+    lib.mla_workspace_bytes.restype = SZ
+    lib.mla_workspace_bytes.argtypes = [I, I, I, I]
+    lib.mla_get_metadata.restype = ctypes.c_int32
+    lib.mla_get_metadata.argtypes = [P, I, I, P, P, P, P]
+    for name in ("mla_decode_with_kvcache", "mla_decode_splitkv"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int32
+        fn.argtypes = [P, I, I, I, I, P, I64, I, I, I, P, I, P, I, P, I, P, F, I, P, P, P, SZ, P, P]
+    lib.mla_combine_splits.restype = ctypes.c_int32
+    lib.mla_combine_splits.argtypes = [P, I, I, I, P, I, P, P, P]
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().mla_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise MLAError(f"{what}: {status_string(code)} ({code})")
+
+
+def _stream_handle() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def num_parts(s_q: int, h_q: int, h_kv: int = 1, device=None) -> int:
+    dev = torch.cuda.current_device() if device is None else torch.device(device).index or 0
+    n = load_library().mla_num_parts(s_q, h_q, h_kv, dev)
+    if n < 0:
+        _check(n, "mla_num_parts")
+    return n
+
+
+def workspace_bytes(b: int, s_q: int, h_q: int, parts: int) -> int:
+    return int(load_library().mla_workspace_bytes(b, s_q, h_q, parts))
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word for the calls below."""
+    return torch.zeros(1, dtype=torch.int32, device=device or torch.cuda.current_device())
+
+
+def check_status(status: torch.Tensor):
+    """Synchronises on the status word and raises if a kernel reported an error."""
+    code = int(status.item())
+    if code != 0:
+        raise MLAError(f"device reported {status_string(code)} ({code})")
+
+
+def get_mla_metadata(cache_seqlens: torch.Tensor, parts: int, status: torch.Tensor | None = None):
+    """Split-KV schedule: returns (metadata int32[parts, 8], num_splits int32[b+1])."""
+    assert cache_seqlens.is_cuda and cache_seqlens.dtype == torch.int32 and cache_seqlens.dim() == 1
+    sl = cache_seqlens.contiguous()
+    b = sl.shape[0]
+    meta = torch.empty((parts, 8), dtype=torch.int32, device=sl.device)
+    nsplit = torch.empty((b + 1,), dtype=torch.int32, device=sl.device)
+    if status is None:
+        status = new_status(sl.device)
+    _check(load_library().mla_get_metadata(sl.data_ptr(), b, parts, meta.data_ptr(), nsplit.data_ptr(),
+                                           status.data_ptr(), _stream_handle()), "mla_get_metadata")
+    return meta, nsplit
+
+
+def entry_stride(kcache: torch.Tensor) -> int:
+    """Elements between consecutive entries of a [num_blocks, 64, h_kv, 576]
+    cache view (576 when dense, 640 for the 256-byte aligned layout)."""
+    nb, bs, h_kv, d = kcache.shape
+    st = kcache.stride()
+    es = st[2] if h_kv > 1 else st[1]
+    if st[3] != 1 or st[1] != h_kv * es or st[0] != bs * st[1]:
+        raise MLAError(f"kcache layout not supported: shape {tuple(kcache.shape)}, strides {st}")
+    return es
+
+
+def mla_decode_with_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
+                            cache_seqlens: torch.Tensor, metadata: torch.Tensor,
+                            num_splits: torch.Tensor, softmax_scale: float, causal: bool = False,
+                            dv: int = D_V, out: torch.Tensor | None = None,
+                            lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            status: torch.Tensor | None = None, combine: bool = True):
+    """MLA decode: returns (out bf16[b, s_q, h_q, 512], lse fp32[b, h_q, s_q]).
+
+    combine=False runs only the split-KV decode kernel (mla_decode_splitkv);
+    combine_splits() must then follow on the same stream."""
+    if not (q.is_cuda and kcache.is_cuda):
+        raise MLAError("q and kcache must be CUDA tensors")
+    if q.dtype != torch.bfloat16 or kcache.dtype != torch.bfloat16:
+        raise MLAError("q and kcache must be bfloat16")
+    if not q.is_contiguous():
+        raise MLAError("q must be contiguous")
+    b, s_q, h_q, d = q.shape
+    nb, bs, h_kv, dk = kcache.shape
+    stride = entry_stride(kcache)
+    bt = block_table.contiguous()
+    sl = cache_seqlens.contiguous()
+    assert bt.dtype == torch.int32 and sl.dtype == torch.int32 and bt.shape[0] == b
+    parts = metadata.shape[0]
+    dev = q.device
+    if out is None:
+        out = torch.empty((b, s_q, h_q, dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((b, h_q, s_q), dtype=torch.float32, device=dev)
+    need = workspace_bytes(b, s_q, h_q, parts)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    lib = load_library()
+    fn = lib.mla_decode_with_kvcache if combine else lib.mla_decode_splitkv
+    rc = fn(
+        q.data_ptr(), b, s_q, h_q, d, kcache.data_ptr(), nb, bs, h_kv, stride, bt.data_ptr(),
+        bt.shape[1], sl.data_ptr(), dv, metadata.data_ptr(), parts, num_splits.data_ptr(),
+        float(softmax_scale), int(bool(causal)), out.data_ptr(), lse.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), status.data_ptr(),
+        _stream_handle())
+    _check(rc, "mla_decode_with_kvcache" if combine else "mla_decode_splitkv")
+    return out, lse
+
+
+def combine_splits(num_splits: torch.Tensor, workspace: torch.Tensor, parts: int, out: torch.Tensor,
+                   lse: torch.Tensor):
+    """The merge half of mla_decode_with_kvcache (mla_combine_splits)."""
+    b, s_q, h_q, _ = out.shape
+    _check(load_library().mla_combine_splits(num_splits.data_ptr(), b, s_q, h_q, workspace.data_ptr(),
+                                             parts, out.data_ptr(), lse.data_ptr(), _stream_handle()),
+           "mla_combine_splits")
+    return out, lse
+
+
+class MLADecoder:
+    """Holds the per-step schedule, scratch and status word for one decode shape.
+
+    plan(cache_seqlens) once per decode step (the schedule is shared by all
+    layers), then __call__ once per layer."""
+
+    def __init__(self, b: int, s_q: int, h_q: int, h_kv: int = 1, device=None, parts: int | None = None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.b, self.s_q, self.h_q, self.h_kv = b, s_q, h_q, h_kv
+        self.parts = parts if parts is not None else num_parts(s_q, h_q, h_kv, self.device)
+        self.workspace = torch.empty((workspace_bytes(b, s_q, h_q, self.parts),), dtype=torch.uint8,
+                                     device=self.device)
+        self.status = new_status(self.device)
+        self.metadata = None
+        self.num_splits = None
+
+    def plan(self, cache_seqlens: torch.Tensor):
+        self.metadata, self.num_splits = get_mla_metadata(cache_seqlens, self.parts, self.status)
+        return self
+
+    def __call__(self, q, kcache, block_table, cache_seqlens, softmax_scale, causal=False, out=None, lse=None):
+        return mla_decode_with_kvcache(q, kcache, block_table, cache_seqlens, self.metadata,
+                                       self.num_splits, softmax_scale, causal, out=out, lse=lse,
+                                       workspace=self.workspace, status=self.status)

@@ -1,0 +1,117 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small shapes are compared element by element on every output row; the five
+named workloads at their full sizes are compared on sampled rows, in the
+launch configuration the benchmark times (the recommended number of parts).
+Tolerance: |d out| <= 1e-2 + 2e-2 |out_oracle| and |d lse| <= 1e-3.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from mla_decode_attention_03_gb300 import ops
+from mla_decode_attention_03_gb300 import workloads as W
+from tests._gpu_helpers import all_rows, assert_matches, run_gpu, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # id, b, s_q, h_q, h_kv, seqlens, stride, causal, parts
+    ("ragged_tails", 5, 1, 128, 1, [1, 63, 64, 65, 700], 576, False, None),
+    ("ragged_tails_split", 5, 1, 128, 1, [1, 63, 64, 65, 700], 576, False, 3),
+    ("causal_two_tiles", 3, 2, 128, 1, [1, 2, 333], 640, True, None),
+    ("causal_64_heads", 4, 2, 64, 1, [100, 200, 64, 5], 640, True, 2),
+    ("kv_groups", 2, 1, 16, 2, [300, 17], 576, False, None),
+    ("three_queries", 3, 3, 32, 1, [130, 3, 64], 576, True, 4),
+    ("empty_sequences", 3, 1, 128, 1, [0, 100, 0], 640, False, None),
+    ("long_split_many", 2, 1, 128, 1, [5000, 3000], 640, False, None),
+    ("h16_many_short", 40, 1, 16, 1, "short", 576, False, None),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_all_rows(case):
+    name, b, s_q, h_q, h_kv, sl, stride, causal, parts = case
+    if sl == "short":
+        sl = list(np.random.default_rng(3).integers(1, 200, size=b))
+    w = W.make(b, s_q, h_q, h_kv, sl, stride=stride, causal=causal, seed=zlib.crc32(name.encode()) % 1000,
+               poison=True)
+    out, lse, _, _ = run_gpu(w, parts=parts)
+    assert_matches(w, out, lse, all_rows(w))
+
+
+@pytest.mark.parametrize("name", ["tiny", "v2lite"])
+def test_named_small_all_rows(name):
+    w = W.named(name)
+    out, lse, _, _ = run_gpu(w)
+    assert_matches(w, out, lse, all_rows(w))
+
+
+@pytest.mark.parametrize("name,stride", [("bench", 576), ("bench", 640), ("mtp", None), ("skewed", None)])
+def test_named_full_size_sampled(name, stride):
+    w = W.named(name, stride=stride)
+    out, lse, _, nsplit = run_gpu(w)
+    last = [w.b - 1, w.s_q - 1, w.h_q - 1]
+    extra = [[0, 0, 0], last]
+    if name == "skewed":  # the two long sequences, every 16th head
+        extra += [[i, 0, h] for i in (0, 1) for h in range(0, w.h_q, 16)]
+    rows = sample_rows(w, 384, seed=1, extra=extra)
+    assert_matches(w, out, lse, rows)
+    # every output row must have been written (no NaN, no untouched garbage)
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(lse).all()
+
+
+def test_stride_576_and_640_identical():
+    w640 = W.make(6, 1, 128, 1, [700, 64, 1, 129, 1000, 333], stride=640, seed=21, poison=True)
+    w576 = W.Workload(**{**w640.__dict__, "kcache_alloc": w640.kcache_alloc[..., :576].contiguous(),
+                         "stride": 576})
+    o1, l1, _, _ = run_gpu(w640, parts=5)
+    o2, l2, _, _ = run_gpu(w576, parts=5)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_page_permutation_identical():
+    w = W.make(4, 2, 128, 1, [300, 129, 64, 1000], causal=True, seed=22, permute=False)
+    o1, l1, _, _ = run_gpu(w, parts=4)
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(w.num_blocks))
+    kc2 = torch.empty_like(w.kcache_alloc)
+    kc2[perm] = w.kcache_alloc
+    bt = w.block_table.clone()
+    bt[bt >= 0] = perm[bt[bt >= 0].long()].int()
+    w2 = W.Workload(**{**w.__dict__, "kcache_alloc": kc2, "block_table": bt})
+    o2, l2, _, _ = run_gpu(w2, parts=4)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("parts", [1, 2, 9, 150])
+def test_split_count_invariance(parts):
+    w = W.make(3, 1, 128, 1, [2000, 513, 4096], stride=640, seed=23)
+    out, lse, meta, nsplit = run_gpu(w, parts=parts)
+    assert_matches(w, out, lse, all_rows(w))
+
+
+def test_bad_block_id_reported_not_faulted():
+    w = W.make(2, 1, 128, 1, [200, 100], seed=24)
+    w.block_table[1, 0] = w.num_blocks + 5  # outside the cache
+    dev = to_device(w)
+    status = ops.new_status()
+    meta, nsplit = ops.get_mla_metadata(dev["cache_seqlens"], 4, status)
+    ops.mla_decode_with_kvcache(dev["q"], dev["kcache"], dev["block_table"], dev["cache_seqlens"],
+                                meta, nsplit, w.softmax_scale, False, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -5
+    # the context is still usable
+    w_ok = W.make(1, 1, 16, 1, [64], seed=25)
+    out, lse, _, _ = run_gpu(w_ok)
+    assert_matches(w_ok, out, lse, all_rows(w_ok))
+
+
+def test_metadata_covers_every_page_once():
+    from tests.test_scheduler import check_schedule
+    sl = np.concatenate([[65536, 65536], np.random.default_rng(2).integers(64, 1024, 62)]).astype(np.int32)
+    for parts in (1, 7, 76, 200):
+        meta, nsplit = ops.get_mla_metadata(torch.from_numpy(sl).cuda(), parts)
+        check_schedule(sl, parts, meta.cpu().numpy(), nsplit.cpu().numpy())
