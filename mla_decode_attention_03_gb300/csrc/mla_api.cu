@@ -160,17 +160,15 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   if (static_cast<int64_t>(s_q) * h_q > 4 * 65535) return MLA_ERR_UNSUPPORTED;
 
   const Shape s = tile_shape(s_q, h_q, h_kv);
-  CUtensorMap q_lat, q_rope, k_lat, k_rope;
+  CUtensorMap q_rope, k_lat, k_rope;
   {
+    // the rope quarter of each CTA's Q columns; the latent half is read by the kernel's threads
     const cuuint64_t row = static_cast<cuuint64_t>(kDimQK) * 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(h_q),
                           static_cast<cuuint64_t>(s_q), static_cast<cuuint64_t>(b)};
     cuuint64_t strides[3] = {row, row * h_q, row * h_q * s_q};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(s.heads_per_kv), static_cast<cuuint32_t>(s.q_per_tile), 1};
-    mla_status_t r = encode(&q_lat, 4, const_cast<void*>(q), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (r != MLA_OK) return r;
-    box[0] = 32;
-    r = encode(&q_rope, 4, const_cast<void*>(q), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    cuuint32_t box[4] = {32, static_cast<cuuint32_t>(s.heads_per_kv), static_cast<cuuint32_t>(s.q_per_tile), 1};
+    mla_status_t r = encode(&q_rope, 4, const_cast<void*>(q), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     if (r != MLA_OK) return r;
   }
   {
@@ -190,6 +188,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            workspace_o_bytes(b, s_q, h_q, num_parts));
   mla::DecodeParams p;
+  p.q = q;
   p.block_table = block_table;
   p.cache_seqlens = cache_seqlens;
   p.metadata = metadata;
@@ -212,7 +211,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (mla::launch_decode(p, q_lat, q_rope, k_lat, k_rope, num_parts, s.row_tiles, st) != cudaSuccess)
+  if (mla::launch_decode(p, q_rope, k_lat, k_rope, num_parts, s.row_tiles, st) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (!with_combine) return MLA_OK;
   return mla_combine_splits(num_splits, b, s_q, h_q, workspace, num_parts, out, lse, stream);

@@ -20,9 +20,17 @@
 //    identical softmax decisions).  Each CTA then multiplies P by its own V half
 //    (its latent dims are exactly half of V), so O [128 x 512] fp32 -- which
 //    would fill all of one SM's tensor memory -- is split 256 columns per SM.
+//  * Tensor memory per CTA: O half (256 columns), two S buffers (64 columns
+//    each; P overwrites S in place as packed bf16 and feeds PV straight from
+//    tensor memory), and the CTA's latent half of Q (128 columns, bf16), so
+//    QK reads only K from shared memory.  Shared memory holds 4 K stages, two
+//    exchange slots and the rope quarter of Q.
 //  * Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma and owns
 //    tensor memory, warps 2-5 do the online softmax (one query row per thread)
-//    and the epilogue.  All hand-offs are mbarriers; every wait is bounded.
+//    and the epilogue, warps 6-9 stage each sequence's Q into tensor memory.
+//    All hand-offs are mbarriers; every wait is bounded.
+//  * tcgen05.mma operations of one thread execute in issue order, so QK(n+2)
+//    is issued right behind PV(n) into the buffer PV(n) reads P from.
 //  * Scores use exp2 with scale*log2(e) folded in; the running max is only
 //    moved (and O rescaled in tensor memory) when it grows by more than 8, so
 //    rescaling is rare.
@@ -34,37 +42,29 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
-constexpr int kQChunk = kRowsPerTile * 128;  // 128 rows x 64 bf16 (128B swizzle)
-constexpr int kQRope = kRowsPerTile * 64;    // 128 rows x 32 bf16 (64B swizzle)
-constexpr int kQBytes = 4 * kQChunk + kQRope;
-constexpr int kKChunk = kPage * 128;
-constexpr int kKRope = kPage * 64;
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr int kKChunk = kPage * 128;           // 64 tokens x 64 dims bf16 (128B swizzle)
+constexpr int kKRope = kPage * 64;             // 64 tokens x 32 dims bf16 (64B swizzle)
 constexpr int kKStage = 4 * kKChunk + kKRope;  // 36864 bytes: this CTA's 288 dims of a page
-constexpr int kPBuf = kRowsPerTile * 128;      // P: 128 rows x 64 bf16
-constexpr int kXRow = 272;                     // exchange row pitch (64 fp32 + 16 B pad)
-constexpr int kXBytes = kRowsPerTile * kXRow;
+constexpr int kXSlot = kRowsPerTile * 256;     // exchange: 128 rows x 64 fp32
+constexpr int kQRope = kRowsPerTile * 64;      // Q rope quarter: 128 rows x 32 bf16 (64B swizzle)
 
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffP = kOffK + kStages * kKStage;
-constexpr int kOffX = kOffP + 2 * kPBuf;
-constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kOffK = 0;
+constexpr int kOffX = kOffK + kStages * kKStage;
+constexpr int kOffQR = kOffX + 2 * kXSlot;
+constexpr int kOffBar = kOffQR + kQRope;
 
 // barrier slots
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + kStages;
 constexpr int kBarQFull = kBarEmpty + kStages;
 constexpr int kBarQEmpty = kBarQFull + 1;
-constexpr int kBarSFull = kBarQEmpty + 1;   // 2
-constexpr int kBarSEmpty = kBarSFull + 2;   // 2
-constexpr int kBarPFull = kBarSEmpty + 2;   // 2
-constexpr int kBarPEmpty = kBarPFull + 2;   // 2
-constexpr int kBarOFull = kBarPEmpty + 2;
-constexpr int kBarXFull = kBarOFull + 1;
-constexpr int kBarXEmpty = kBarXFull + 1;
-constexpr int kBarDone = kBarXEmpty + 1;
+constexpr int kBarSFull = kBarQEmpty + 1;  // 2
+constexpr int kBarPFull = kBarSFull + 2;   // 2
+constexpr int kBarOFull = kBarPFull + 2;
+constexpr int kBarXFull = kBarOFull + 1;   // 2
+constexpr int kBarDone = kBarXFull + 2;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -72,8 +72,9 @@ constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;     // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;   // S buffers: [256, 320), [320, 384)
+constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
+constexpr uint32_t kTmemS = 256;  // S/P buffers: [256, 320), [320, 384)
+constexpr uint32_t kTmemQ = 384;  // Q latent half, bf16 pairs: [384, 512)
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
@@ -81,8 +82,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // --------------------------------------------------------------- schedule
-// One (sequence, page range) piece of a part, and a page-by-page walk over
-// all pieces of a part.
+// A page-by-page walk over the (sequence, page range) segments of one part.
 struct PageWalk {
   const int32_t* seqlens;
   int max_blocks;
@@ -125,6 +125,9 @@ struct PageWalk {
   __device__ __forceinline__ bool last() const { return p == p_end - 1; }
   __device__ __forceinline__ void advance() {
     if (++p < p_end) return;
+    next_segment();
+  }
+  __device__ __forceinline__ void next_segment() {
     ++i;
     p_begin = 0;
     k = 0;
@@ -145,11 +148,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Offset of 16-byte chunk c of exchange row r (XOR swizzle: conflict-free for
+// both the remote writer and the local reader).
+__device__ __forceinline__ uint32_t x_chunk(int r, int c) {
+  return static_cast<uint32_t>(r * 256 + ((c ^ (r & 15)) << 4));
+}
+
 // ----------------------------------------------------------------- kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_constant__ CUtensorMap q_rope,
-                  const __grid_constant__ CUtensorMap k_lat, const __grid_constant__ CUtensorMap k_rope,
-                  const DecodeParams P) {
+mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_constant__ CUtensorMap k_lat,
+                  const __grid_constant__ CUtensorMap k_rope, const DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -176,17 +184,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
     }
-    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQFull), 1 + 4);  // rope TMA + the 4 Q-staging warps
     mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarSEmpty + s), 4);
       mbar_init(bar(kBarPFull + s), 4);
-      mbar_init(bar(kBarPEmpty + s), 1);
+      mbar_init(bar(kBarXFull + s), 1);
     }
     mbar_init(bar(kBarOFull), 1);
-    mbar_init(bar(kBarXFull), 1);
-    mbar_init(bar(kBarXEmpty), 4);
     mbar_init(bar(kBarDone), 1);
     fence_mbar_init();
   }
@@ -194,14 +199,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2 && rows_valid < kRowsPerTile) {
-    // Rows the Q tile does not fill stay zero (their outputs are discarded).
-    const int t = tid - 64;
-    for (int c = 0; c < 4; ++c)
-      for (int off = rows_valid * 128 + t * 16; off < kQChunk; off += 128 * 16)
-        *reinterpret_cast<uint4*>(gbase + kOffQ + c * kQChunk + off) = make_uint4(0, 0, 0, 0);
+  if (warp >= 6 && rows_valid < kRowsPerTile) {
+    // Rope rows the Q tile does not fill stay zero (their outputs are discarded).
+    const int t = tid - 192;
     for (int off = rows_valid * 64 + t * 16; off < kQRope; off += 128 * 16)
-      *reinterpret_cast<uint4*>(gbase + kOffQ + 4 * kQChunk + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(gbase + kOffQR + off) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   tc_fence_before_sync();
@@ -212,28 +214,24 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
   if (warp == 0) {
     // ================================================= TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&q_lat);
       tma_prefetch_desc(&q_rope);
       tma_prefetch_desc(&k_lat);
       tma_prefetch_desc(&k_rope);
       const uint64_t evict_first = l2_policy_evict_first();
       const int dim_lat = 256 * static_cast<int>(rank);
       const int dim_rope = 512 + 32 * static_cast<int>(rank);
-      const uint32_t q_bytes = static_cast<uint32_t>(rows_valid) * 288u * 2u;  // this CTA's 288 dims per row
       PageWalk w;
       w.start(meta, P.cache_seqlens, P.max_blocks);
-      int n = 0, qn = 0;
+      int n = 0, seg = 0;
       bool ok = true;
       while (w.valid && ok) {
         if (w.first()) {
-          ok = mbar_wait(bar(kBarQEmpty), (qn & 1) ^ 1, abort_flag);
+          ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar(kBarQFull), q_bytes);
-          const int h0 = g * P.heads_per_kv, j0 = tile * P.q_per_tile;
-          for (int c = 0; c < 4; ++c)
-            tma_load_4d(base + kOffQ + c * kQChunk, &q_lat, bar(kBarQFull), dim_lat + 64 * c, h0, j0, w.i);
-          tma_load_4d(base + kOffQ + 4 * kQChunk, &q_rope, bar(kBarQFull), dim_rope, h0, j0, w.i);
-          ++qn;
+          mbar_arrive_expect_tx(bar(kBarQFull), static_cast<uint32_t>(rows_valid) * 64u);
+          tma_load_4d(base + kOffQR, &q_rope, bar(kBarQFull), dim_rope, g * P.heads_per_kv,
+                      tile * P.q_per_tile, w.i);
+          ++seg;
         }
         int phys = __ldg(P.block_table + static_cast<int64_t>(w.i) * P.max_blocks + w.p);
         if (phys < 0 || phys >= P.num_blocks) {
@@ -246,6 +244,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
         mbar_arrive_expect_tx(bar(kBarFull + st), kKStage);
         const uint32_t dst = base + kOffK + st * kKStage;
         const int row = phys * kPage;
+#pragma unroll
         for (int c = 0; c < 4; ++c)
           tma_load_3d_hint(dst + c * kKChunk, &k_lat, bar(kBarFull + st), dim_lat + 64 * c, g, row,
                            evict_first);
@@ -258,49 +257,49 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
         // let the copies already issued land before this CTA can exit
         for (int m = (n > kStages ? n - kStages : 0); m < n; ++m)
           drain_wait(bar(kBarFull + m % kStages), (m / kStages) & 1);
-        if (qn > 0) drain_wait(bar(kBarQFull), (qn - 1) & 1);
+        if (seg > 0) drain_wait(bar(kBarQFull), (seg - 1) & 1);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================================= MMA issuer
     if (lane == 0) {
+      // Descriptors are built once; per MMA only a constant offset (>> 4) is added.
+      const uint64_t d_klat = smem_desc(base + kOffK, 16, 1024, kSwizzle128B);
+      const uint64_t d_krope = smem_desc(base + kOffK + 4 * kKChunk, 16, 512, kSwizzle64B);
+      const uint64_t d_qrope = smem_desc(base + kOffQR, 16, 512, kSwizzle64B);
+      // V = this CTA's 256 latent dims of the page, read MN-major:
+      // 64-dim column blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
+      const uint64_t d_v = smem_desc(base + kOffK, kKChunk, 1024, kSwizzle128B);
       PageWalk wq, wp;
       wq.start(meta, P.cache_seqlens, P.max_blocks);
       wp = wq;
-      int nq = 0, np = 0, qn = 0;
+      int nq = 0, np = 0, qseg = 0;
       bool ok = true;
       auto issue_qk = [&](const PageWalk& w) -> bool {
         if (w.first()) {
-          if (!mbar_wait(bar(kBarQFull), qn & 1, abort_flag)) return false;
-          ++qn;
+          if (!mbar_wait(bar(kBarQFull), qseg & 1, abort_flag)) return false;
+          ++qseg;
         }
         const int st = nq % kStages;
         if (!mbar_wait(bar(kBarFull + st), (nq / kStages) & 1, abort_flag)) return false;
-        const int sb = nq & 1;
-        if (!mbar_wait(bar(kBarSEmpty + sb), ((nq >> 1) & 1) ^ 1, abort_flag)) return false;
         tc_fence_after_sync();
-        const uint32_t q_s = base + kOffQ;
-        const uint32_t k_s = base + kOffK + st * kKStage;
-        const uint32_t d = tmem + kTmemS + 64u * sb;
-        uint32_t acc = 0;
+        const uint32_t d = tmem + kTmemS + 64u * (nq & 1);
+        const uint64_t koff = static_cast<uint64_t>((st * kKStage) >> 4);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = smem_desc(q_s + c * kQChunk + ks * 32, 16, 1024, kSwizzle128B);
-            const uint64_t b = smem_desc(k_s + c * kKChunk + ks * 32, 16, 1024, kSwizzle128B);
-            umma_bf16(d, a, b, kIdescQK, acc);
-            acc = 1;
+            umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * ks,
+                         d_klat + koff + static_cast<uint64_t>((c * kKChunk + ks * 32) >> 4), kIdescQK,
+                         (c | ks) != 0);
           }
         }
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t a = smem_desc(q_s + 4 * kQChunk + ks * 32, 16, 512, kSwizzle64B);
-          const uint64_t b = smem_desc(k_s + 4 * kKChunk + ks * 32, 16, 512, kSwizzle64B);
-          umma_bf16(d, a, b, kIdescQK, 1);
-        }
-        umma_commit(bar(kBarSFull + sb));
+        for (int ks = 0; ks < 2; ++ks)
+          umma_bf16(d, d_qrope + static_cast<uint64_t>((ks * 32) >> 4),
+                    d_krope + koff + static_cast<uint64_t>((ks * 32) >> 4), kIdescQK, 1);
+        umma_commit(bar(kBarSFull + (nq & 1)));
         if (w.last()) umma_commit(bar(kBarQEmpty));
         ++nq;
         return true;
@@ -310,39 +309,28 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
         if (!mbar_wait(bar(kBarPFull + pb), (np >> 1) & 1, abort_flag)) return false;
         tc_fence_after_sync();
         const int st = np % kStages;
-        const uint32_t k_s = base + kOffK + st * kKStage;
-        const uint32_t p_s = base + kOffP + pb * kPBuf;
+        const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
         const uint32_t first = w.first() ? 1u : 0u;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = smem_desc(p_s + ks * 32, 16, 1024, kSwizzle128B);
-          // V = this CTA's 256 latent dims of the page, read MN-major:
-          // 64-dim column blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
-          const uint64_t b = smem_desc(k_s + ks * 2048, kKChunk, 1024, kSwizzle128B);
-          umma_bf16(tmem + kTmemO, a, b, kIdescPV, (first && ks == 0) ? 0u : 1u);
-        }
-        umma_commit(bar(kBarPEmpty + pb));
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + 64u * pb + 8 * ks,
+                       d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
+                       (first && ks == 0) ? 0u : 1u);
         umma_commit(bar(kBarEmpty + st));
         umma_commit(bar(kBarOFull));
         ++np;
         return true;
       };
-      if (wq.valid) {
+      // QK runs two pages ahead of PV: one S buffer per page in flight.
+      for (int a = 0; a < 2 && ok && wq.valid; ++a) {
         ok = issue_qk(wq);
         wq.advance();
       }
       while (ok && wp.valid) {
-        const bool next_same_seg = wq.valid && !wq.first();
-        if (next_same_seg) {
-          ok = issue_qk(wq);
-          wq.advance();
-          if (!ok) break;
-        }
         ok = issue_pv(wp);
         wp.advance();
-        if (!ok) break;
-        if (wq.valid && !next_same_seg) {
-          ok = issue_qk(wq);
+        if (ok && wq.valid) {
+          ok = issue_qk(wq);  // into the buffer PV just read P from (in-order execution)
           wq.advance();
         }
       }
@@ -351,17 +339,15 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
       drain_wait(bar(kBarDone), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ================================================= softmax + epilogue
     const int quad = warp & 3;
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const bool leader = (tid == 64);
-    const uint32_t x_row = base + kOffX + row * kXRow;
-    const uint32_t peer_x_row = cluster_map(x_row, peer);
-    const uint32_t peer_x_full = cluster_map(bar(kBarXFull), peer);
-    const uint32_t peer_x_empty = cluster_map(bar(kBarXEmpty), peer);
-    uint8_t* const p_gen = gbase + kOffP;
+    const uint32_t peer_x = cluster_map(base + kOffX, peer);
+    const uint32_t peer_x_full0 = cluster_map(bar(kBarXFull), peer);
+    const uint32_t peer_x_full1 = cluster_map(bar(kBarXFull + 1), peer);
 
     // row -> (query position, head)
     const int jj = row / P.heads_per_kv;
@@ -371,6 +357,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
     const bool row_live = (row < rows_valid) && (j < P.s_q);
     const int rows_total = P.s_q * P.h_q;
     const int row_in_seq = j * P.h_q + h;
+    const float c_log2 = P.scale_log2;
 
     PageWalk w;
     w.start(meta, P.cache_seqlens, P.max_blocks);
@@ -387,57 +374,60 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
         l_run = 0.f;
       }
       const int sb = n & 1;
-      if (leader) mbar_arrive_expect_tx(bar(kBarXFull), kRowsPerTile * 256);
+      const uint32_t par = (n >> 1) & 1;
+      if (leader) mbar_arrive_expect_tx(bar(kBarXFull + sb), kXSlot);
 
       // ---- own partial scores out of tensor memory
       uint32_t s0[32], s1[32];
-      ok = mbar_wait(bar(kBarSFull + sb), (n >> 1) & 1, abort_flag);
+      ok = mbar_wait(bar(kBarSFull + sb), par, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
-      tmem_ld32(tmem + lane_off + kTmemS + 64u * sb, s0);
-      tmem_ld32(tmem + lane_off + kTmemS + 64u * sb + 32, s1);
+      const uint32_t t_s = tmem + lane_off + kTmemS + 64u * sb;
+      tmem_ld32(t_s, s0);
+      tmem_ld32(t_s + 32, s1);
       tmem_wait_ld2(s0, s1);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
 
-      // ---- swap partials with the peer CTA
-      ok = mbar_wait<true>(bar(kBarXEmpty), (n & 1) ^ 1, abort_flag);
-      if (!ok) break;
+      // ---- send them to the peer CTA, take the peer's
+      {
+        const uint32_t dst = peer_x + sb * kXSlot;
+        const uint32_t xb = sb ? peer_x_full1 : peer_x_full0;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(peer_x_row + 16 * c, s0[4 * c], s0[4 * c + 1], s0[4 * c + 2], s0[4 * c + 3],
-                    peer_x_full);
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(dst + x_chunk(row, c), s0[4 * c], s0[4 * c + 1], s0[4 * c + 2], s0[4 * c + 3], xb);
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(peer_x_row + 128 + 16 * c, s1[4 * c], s1[4 * c + 1], s1[4 * c + 2],
-                    s1[4 * c + 3], peer_x_full);
-      ok = mbar_wait<true>(bar(kBarXFull), n & 1, abort_flag);
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(dst + x_chunk(row, 8 + c), s1[4 * c], s1[4 * c + 1], s1[4 * c + 2], s1[4 * c + 3], xb);
+      }
+      ok = mbar_wait(bar(kBarXFull + sb), par, abort_flag);
       if (!ok) break;
       float x[64];
       {
-        const float4* xr = reinterpret_cast<const float4*>(gbase + kOffX + row * kXRow);
+        const uint8_t* xr = gbase + kOffX + sb * kXSlot;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float4 v = xr[c];
+          const float4 v = *reinterpret_cast<const float4*>(xr + x_chunk(row, c));
           const uint32_t* src = (c < 8) ? &s0[4 * c] : &s1[4 * (c - 8)];
-          x[4 * c + 0] = __uint_as_float(src[0]) + v.x;
-          x[4 * c + 1] = __uint_as_float(src[1]) + v.y;
-          x[4 * c + 2] = __uint_as_float(src[2]) + v.z;
-          x[4 * c + 3] = __uint_as_float(src[3]) + v.w;
+          x[4 * c + 0] = (__uint_as_float(src[0]) + v.x) * c_log2;
+          x[4 * c + 1] = (__uint_as_float(src[1]) + v.y) * c_log2;
+          x[4 * c + 2] = (__uint_as_float(src[2]) + v.z) * c_log2;
+          x[4 * c + 3] = (__uint_as_float(src[3]) + v.w) * c_log2;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(peer_x_empty);
 
       // ---- online softmax for this row and page
       const int t0 = w.p * kPage;
-      float mx = -INFINITY;
+      if (t0 + kPage > lim) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        x[c] = (t0 + c < lim) ? x[c] * P.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[c]);
+        for (int c = 0; c < 64; ++c)
+          if (t0 + c >= lim) x[c] = -INFINITY;
       }
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = x[u];
+#pragma unroll
+      for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx);
       float alpha = 1.f;
       if (m_new > m_run + kRescaleThreshold) {
@@ -460,35 +450,27 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(tmem + lane_off + kTmemO + 32 * c, o);
         }
-        tmem_wait_st();
       }
 
-      // ---- P (bf16) into the swizzled operand buffer
-      const int pb = n & 1;
-      ok = mbar_wait(bar(kBarPEmpty + pb), ((n >> 1) & 1) ^ 1, abort_flag);
-      if (!ok) break;
-      float rsum = 0.f;
-      uint8_t* prow = p_gen + pb * kPBuf + row * 128;
+      // ---- P (bf16 pairs) over S in tensor memory
+      uint32_t pk[32];
+      float sum8[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float e[8];
+      for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          e[u] = ex2_approx(x[8 * c + u] - m_sub);
-          rsum += e[u];
-        }
-        uint4 v;
-        v.x = pack_bf16x2(e[0], e[1]);
-        v.y = pack_bf16x2(e[2], e[3]);
-        v.z = pack_bf16x2(e[4], e[5]);
-        v.w = pack_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = v;
+      for (int c = 0; c < 32; ++c) {
+        const float e0 = ex2_approx(x[2 * c] - m_sub);
+        const float e1 = ex2_approx(x[2 * c + 1] - m_sub);
+        sum8[c & 7] += e0 + e1;
+        pk[c] = pack_bf16x2(e0, e1);
       }
-      l_run = l_run * alpha + rsum;
-      fence_proxy_async_smem();
+      tmem_st32(t_s, pk);
+      tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
+      const float rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      l_run = l_run * alpha + rsum;
 
       // ---- epilogue at the end of a segment
       if (w.last()) {
@@ -542,6 +524,54 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
       w.advance();
     }
     if (!ok) raise_status(P.status, kStatusTimeout);
+  } else {
+    // ================================================= Q staging into tensor memory
+    const int quad = warp & 3;
+    const int row = 32 * quad + static_cast<int>(lane);
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    const int jj = row / P.heads_per_kv;
+    const int hh = row - jj * P.heads_per_kv;
+    const int j = tile * P.q_per_tile + jj;
+    const int h = g * P.heads_per_kv + hh;
+    const bool row_live = (row < rows_valid) && (j < P.s_q);
+    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(P.q);
+
+    PageWalk w;
+    w.start(meta, P.cache_seqlens, P.max_blocks);
+    int seg = 0;
+    bool ok = true;
+    while (w.valid && ok) {
+      // this CTA's 256 latent dims of the row, as 128 bf16 pairs
+      uint32_t qr[128];
+      if (row_live) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            qbase + ((static_cast<int64_t>(w.i) * P.s_q + j) * P.h_q + h) * kDimQK + 256 * rank);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const uint4 v = ld_global_nc_v4(src + 16 * k);
+          qr[4 * k + 0] = v.x;
+          qr[4 * k + 1] = v.y;
+          qr[4 * k + 2] = v.z;
+          qr[4 * k + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 128; ++k) qr[k] = 0u;
+      }
+      ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tmem_st32(tmem + lane_off + kTmemQ + 32 * k, *reinterpret_cast<const uint32_t(*)[32]>(qr + 32 * k));
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarQFull));
+      ++seg;
+      w.next_segment();
+    }
+    if (!ok) raise_status(P.status, kStatusTimeout);
   }
 
   // ---- teardown: everyone is done with tensor memory and with the peer
@@ -558,9 +588,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_lat, const __grid_consta
 
 int decode_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_lat, const CUtensorMap& q_rope,
-                          const CUtensorMap& k_lat, const CUtensorMap& k_rope, int num_parts,
-                          int row_tiles, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_rope, const CUtensorMap& k_lat,
+                          const CUtensorMap& k_rope, int num_parts, int row_tiles, cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -571,7 +600,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_lat, const
     configured_device = dev;
   }
   dim3 grid(2 * num_parts, row_tiles, p.h_kv);
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_lat, q_rope, k_lat, k_rope, p);
+  mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_rope, k_lat, k_rope, p);
   return cudaGetLastError();
 }
 

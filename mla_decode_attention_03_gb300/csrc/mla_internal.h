@@ -25,6 +25,7 @@ enum : int32_t {
 };
 
 struct DecodeParams {
+  const void* q;                 // bf16 [b, s_q, h_q, 576]
   const int32_t* block_table;    // [b, max_blocks]
   const int32_t* cache_seqlens;  // [b]
   const int32_t* metadata;       // [num_parts, kMetaInts]
@@ -54,9 +55,8 @@ struct CombineParams {
 };
 
 int decode_smem_bytes();
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_lat, const CUtensorMap& q_rope,
-                          const CUtensorMap& k_lat, const CUtensorMap& k_rope, int num_parts,
-                          int row_tiles, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_rope, const CUtensorMap& k_lat,
+                          const CUtensorMap& k_rope, int num_parts, int row_tiles, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, int32_t* metadata,
                             int32_t* num_splits, int32_t* status, cudaStream_t stream);
