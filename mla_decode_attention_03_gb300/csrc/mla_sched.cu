@@ -14,103 +14,156 @@
 namespace mla {
 namespace {
 
-// Greedy balanced cut of the (sequence, page) order into num_parts contiguous
-// parts.  Every (sequence, part) segment costs its pages plus kSegmentCost;
-// each part takes about (total + split overheads)/num_parts.  Output per part:
+// Balanced cut of the (sequence, page) order into num_parts contiguous parts.
+//
+// Cost axis: sequence i with n_i > 0 pages occupies [C_i, C_i + n_i + F), where
+// C is the exclusive prefix sum of the widths and the first F = kSegmentCost
+// units stand for the fixed cost of a segment (Q load, epilogue).  Part q takes
+// the cost range [q*per, (q+1)*per), per = max(ceil(total/P), F + kMinPartPages).
+// A cut at cost x falls in sequence i = max{i : C_i <= x}, at page
+// max(0, x - C_i - F); cuts inside a sequence's first F units therefore start
+// the part at that sequence's first page.  Every quantity below is a closed
+// form of C and per, so all parts and sequences are computed in parallel.
+//
+// Output per part:
 //   meta[0] = first sequence, meta[1] = first page in it,
 //   meta[2] = last sequence,  meta[3] = end page (exclusive) in the last one,
 //   meta[4] = split index of the first segment within its sequence.
 // An empty part has meta[0] > meta[2].  num_splits[b+1] is the exclusive
-// prefix sum of the number of segments of each sequence.
-__global__ void __launch_bounds__(256) mla_metadata_kernel(const int32_t* __restrict__ seqlens, int b,
-                                                           int num_parts, int32_t* __restrict__ meta,
-                                                           int32_t* __restrict__ num_splits,
-                                                           int32_t* __restrict__ status) {
-  extern __shared__ int32_t sh[];  // [0, b): pages per sequence; [b, 2b): segments per sequence
-  int32_t* pages = sh;
-  int32_t* segs = sh + b;
-  for (int i = threadIdx.x; i < b; i += blockDim.x) {
-    const int L = seqlens[i];
-    if (L < 0) atomicExch(status, kStatusBadSeqlen);
-    pages[i] = L > 0 ? (L + kPage - 1) / kPage : 0;
-    segs[i] = 0;
+// prefix sum of the number of segments (pieces) of each sequence.
+constexpr int kMetaThreads = 512;
+
+__device__ __forceinline__ int64_t width_of(int L) {
+  const int64_t n = L > 0 ? (static_cast<int64_t>(L) + kPage - 1) / kPage : 0;
+  return n > 0 ? n + kSegmentCost : 0;
+}
+
+// The last i in [0, b) with C[i] <= x (C[0] = 0 <= x).
+__device__ __forceinline__ int seq_at(const int64_t* C, int b, int64_t x) {
+  int l = 0, r = b;
+  while (l < r) {
+    const int m = (l + r) >> 1;
+    if (C[m] <= x) l = m + 1; else r = m;
+  }
+  return l - 1;
+}
+
+// Block-wide exclusive scan of one value per thread; returns the block total in *total.
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* warp_buf, T* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  T incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_buf[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    T w = lane < kMetaThreads / 32 ? warp_buf[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kMetaThreads / 32) warp_buf[lane] = w;  // inclusive per-warp prefix
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    long long total = 0;
-    for (int i = 0; i < b; ++i)
-      if (pages[i] > 0) total += pages[i] + kSegmentCost;
-    // Each part boundary that falls inside a sequence adds one more segment
-    // (and its fixed cost); budget for up to num_parts-1 of them.
-    const long long estimate = total + static_cast<long long>(kSegmentCost) * (num_parts - 1);
-    long long per_part = (estimate + num_parts - 1) / num_parts;
-    if (per_part < kSegmentCost + kMinPartPages) per_part = kSegmentCost + kMinPartPages;
+  const T warp_excl = wid > 0 ? warp_buf[wid - 1] : T(0);
+  *total = warp_buf[kMetaThreads / 32 - 1];
+  __syncthreads();
+  return warp_excl + incl - v;
+}
 
-    // Part q ends near cumulative cost (q+1)*per_part, so a part that stops a
-    // little short does not push the shortfall onto the last part.
-    long long consumed = 0;
-    int i = 0, p = 0, k = 0, part = 0;
-    while (i < b && pages[i] == 0) ++i;
-    for (; part < num_parts && i < b; ++part) {
-      int32_t* m = meta + part * kMetaInts;
-      m[0] = i;
-      m[1] = p;
-      m[4] = k;
-      m[5] = m[6] = m[7] = 0;
-      const bool last_part = (part == num_parts - 1);
-      long long budget = (part + 1) * per_part - consumed;
-      int last_i = i, last_end = p;
-      while (i < b) {
-        if (pages[i] == 0) {
-          ++i;
-          continue;
-        }
-        if (!last_part && budget < kSegmentCost + 1) break;
-        const long long need = kSegmentCost + (pages[i] - p);
-        if (last_part || need <= budget) {
-          budget -= need;
-          consumed += need;
-          segs[i] = k + 1;
-          last_i = i;
-          last_end = pages[i];
-          ++i;
-          p = 0;
-          k = 0;
-        } else {
-          const int take = static_cast<int>(budget - kSegmentCost);  // >= 1
-          consumed += budget;
-          segs[i] = k + 1;
-          last_i = i;
-          p += take;
-          last_end = p;
-          ++k;
-          break;
-        }
-      }
-      if (last_end == m[1] && last_i == m[0]) {
-        m[0] = 1;  // nothing placed: empty part
-        m[2] = 0;
-      } else {
-        m[2] = last_i;
-      }
-      m[3] = last_end;
-      while (i < b && pages[i] == 0) ++i;
-    }
-    for (; part < num_parts; ++part) {
-      int32_t* m = meta + part * kMetaInts;
-      m[0] = 1;
-      m[1] = 0;
-      m[2] = 0;
-      m[3] = 0;
-      m[4] = m[5] = m[6] = m[7] = 0;
-    }
-    int acc = 0;
-    num_splits[0] = 0;
-    for (int s = 0; s < b; ++s) {
-      acc += segs[s];
-      num_splits[s + 1] = acc;
-    }
+__global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_t* __restrict__ seqlens, int b,
+                                                                    int num_parts, int32_t* __restrict__ meta,
+                                                                    int32_t* __restrict__ num_splits,
+                                                                    int32_t* __restrict__ status) {
+  extern __shared__ int64_t C[];  // [b + 1]: cost prefix
+  __shared__ int64_t buf64[kMetaThreads / 32];
+  __shared__ int32_t buf32[kMetaThreads / 32];
+  const int tid = threadIdx.x;
+  const int chunk = (b + kMetaThreads - 1) / kMetaThreads;
+  const int lo = min(b, tid * chunk), hi = min(b, lo + chunk);
+
+  int64_t local = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int L = seqlens[i];
+    if (L < 0) atomicExch(status, kStatusBadSeqlen);
+    local += width_of(L);
   }
+  int64_t total = 0;
+  int64_t run = block_exclusive_scan<int64_t>(local, buf64, &total);
+  for (int i = lo; i < hi; ++i) {
+    C[i] = run;
+    run += width_of(seqlens[i]);
+  }
+  if (tid == 0) C[b] = total;
+  __syncthreads();
+
+  int64_t per = (total + num_parts - 1) / num_parts;
+  if (per < kSegmentCost + kMinPartPages) per = kSegmentCost + kMinPartPages;
+  auto pages = [&](int i) -> int { return static_cast<int>(C[i + 1] - C[i] - kSegmentCost); };
+
+  for (int q = tid; q < num_parts; q += kMetaThreads) {
+    int32_t* m = meta + q * kMetaInts;
+    m[5] = m[6] = m[7] = 0;
+    const int64_t x0 = static_cast<int64_t>(q) * per;
+    const int64_t x1 = x0 + per;
+    if (x0 >= total) {
+      m[0] = 1; m[1] = 0; m[2] = 0; m[3] = 0; m[4] = 0;
+      continue;
+    }
+    const int i0 = seq_at(C, b, x0);
+    const int64_t o0 = x0 - C[i0] - kSegmentCost;
+    const int p0 = o0 > 0 ? static_cast<int>(o0) : 0;
+    int i1, pe1;
+    bool empty = false;
+    if (x1 >= total) {
+      i1 = seq_at(C, b, total - 1);
+      pe1 = pages(i1);
+    } else {
+      const int ie = seq_at(C, b, x1);
+      const int64_t oe = x1 - C[ie] - kSegmentCost;
+      if (oe > 0) {
+        i1 = ie;
+        pe1 = static_cast<int>(oe);
+      } else if (ie == i0 && p0 == 0) {
+        empty = true;  // both cuts fall before the first page of the same sequence
+        i1 = pe1 = 0;
+      } else {
+        i1 = seq_at(C, b, C[ie] - 1);  // ends with the previous sequence
+        pe1 = pages(i1);
+      }
+    }
+    if (empty) {
+      m[0] = 1; m[1] = 0; m[2] = 0; m[3] = 0; m[4] = 0;
+      continue;
+    }
+    m[0] = i0;
+    m[1] = p0;
+    m[2] = i1;
+    m[3] = pe1;
+    // cuts inside sequence i0 at or before x0: multiples of per in (C + F, x0]
+    const int64_t first = (C[i0] + kSegmentCost) / per;
+    m[4] = p0 > 0 ? static_cast<int>(q - first) : 0;
+  }
+
+  // pieces per sequence: 1 + the cuts strictly inside its pages
+  int32_t local_segs = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int64_t w = C[i + 1] - C[i];
+    if (w > 0) local_segs += 1 + static_cast<int32_t>(max(int64_t(0), (C[i] + w - 1) / per - (C[i] + kSegmentCost) / per));
+  }
+  int32_t seg_total = 0;
+  int32_t srun = block_exclusive_scan<int32_t>(local_segs, buf32, &seg_total);
+  for (int i = lo; i < hi; ++i) {
+    num_splits[i] = srun;
+    const int64_t w = C[i + 1] - C[i];
+    if (w > 0) srun += 1 + static_cast<int32_t>(max(int64_t(0), (C[i] + w - 1) / per - (C[i] + kSegmentCost) / per));
+  }
+  if (tid == 0) num_splits[b] = seg_total;
 }
 
 // One warp per (sequence, query row).  Sequences with a single split were
@@ -179,18 +232,18 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams P)
 
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, int32_t* metadata,
                             int32_t* num_splits, int32_t* status, cudaStream_t stream) {
-  const size_t smem = sizeof(int32_t) * 2 * static_cast<size_t>(b);
+  const size_t smem = sizeof(int64_t) * (static_cast<size_t>(b) + 1);
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(int32_t) * 2 * kMaxMetadataBatch));
+                             static_cast<int>(sizeof(int64_t) * (kMaxMetadataBatch + 1)));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  mla_metadata_kernel<<<1, 256, smem, stream>>>(cache_seqlens, b, num_parts, metadata, num_splits, status);
+  mla_metadata_kernel<<<1, kMetaThreads, smem, stream>>>(cache_seqlens, b, num_parts, metadata, num_splits, status);
   return cudaGetLastError();
 }
 

@@ -4,7 +4,7 @@ No page states how the KV length must be cut -- Flash-Decoding only says that
 it is cut and merged by log-sum-exp -- so any cut that covers every page of
 every sequence exactly once, in order, is correct.  check_schedule() tests
 exactly that, plus the balance the scheduler promises.  A host restatement of
-the greedy cut (host_schedule) lets the CPU suite exercise the properties on
+the cut (host_schedule) lets the CPU suite exercise the properties on
 many shapes and lets the GPU suite require the device output to equal it bit
 for bit (integer work).
 """
@@ -20,54 +20,50 @@ def pages_of(L):
 
 
 def host_schedule(seqlens, parts):
-    """The greedy cut, restated on the host: returns (meta [parts, 8], num_splits [b+1])."""
-    pages = [pages_of(L) for L in seqlens]
-    b = len(pages)
-    total = sum(n + SEGMENT_COST for n in pages if n > 0)
-    estimate = total + SEGMENT_COST * (parts - 1)
-    per = max(-(-estimate // parts), SEGMENT_COST + MIN_PART_PAGES)
+    """The cut, restated on the host: returns (meta [parts, 8], num_splits [b+1]).
+
+    Cost axis: sequence i with n_i > 0 pages occupies [C_i, C_i + n_i + F);
+    part q takes [q*per, (q+1)*per) with per = max(ceil(total/parts), F + MIN);
+    a cut at x lies in the last sequence with C_i <= x, at page max(0, x - C_i - F)."""
+    F = SEGMENT_COST
+    b = len(seqlens)
+    width = [pages_of(L) + F if pages_of(L) > 0 else 0 for L in seqlens]
+    C = np.concatenate([[0], np.cumsum(width)]).astype(np.int64)
+    total = int(C[-1])
+    per = max(-(-total // parts), F + MIN_PART_PAGES)
+
+    def seq_at(x):
+        return int(np.searchsorted(C[:b], x, side="right")) - 1
+
+    def npages(i):
+        return int(C[i + 1] - C[i] - F)
+
     meta = np.zeros((parts, 8), dtype=np.int32)
-    segs = [0] * b
-    consumed, i, p, k, part = 0, 0, 0, 0, 0
-    while i < b and pages[i] == 0:
-        i += 1
-    while part < parts and i < b:
-        m0, m1, m4 = i, p, k
-        last = part == parts - 1
-        budget = (part + 1) * per - consumed
-        last_i, last_end = i, p
-        while i < b:
-            if pages[i] == 0:
-                i += 1
-                continue
-            if not last and budget < SEGMENT_COST + 1:
-                break
-            need = SEGMENT_COST + pages[i] - p
-            if last or need <= budget:
-                budget -= need
-                consumed += need
-                segs[i] = k + 1
-                last_i, last_end = i, pages[i]
-                i, p, k = i + 1, 0, 0
-            else:
-                take = budget - SEGMENT_COST
-                consumed += budget
-                segs[i] = k + 1
-                last_i = i
-                p += take
-                last_end = p
-                k += 1
-                break
-        if last_end == m1 and last_i == m0:
-            meta[part, :5] = [1, m1, 0, last_end, m4]
+    for q in range(parts):
+        x0, x1 = q * per, (q + 1) * per
+        if x0 >= total:
+            meta[q, :5] = [1, 0, 0, 0, 0]
+            continue
+        i0 = seq_at(x0)
+        p0 = max(0, x0 - int(C[i0]) - F)
+        if x1 >= total:
+            i1 = seq_at(total - 1)
+            pe1 = npages(i1)
         else:
-            meta[part, :5] = [m0, m1, last_i, last_end, m4]
-        while i < b and pages[i] == 0:
-            i += 1
-        part += 1
-    while part < parts:
-        meta[part, :5] = [1, 0, 0, 0, 0]
-        part += 1
+            ie = seq_at(x1)
+            oe = x1 - int(C[ie]) - F
+            if oe > 0:
+                i1, pe1 = ie, oe
+            elif ie == i0 and p0 == 0:
+                meta[q, :5] = [1, 0, 0, 0, 0]
+                continue
+            else:
+                i1 = seq_at(int(C[ie]) - 1)
+                pe1 = npages(i1)
+        k0 = q - (int(C[i0]) + F) // per if p0 > 0 else 0
+        meta[q, :5] = [i0, p0, i1, pe1, k0]
+    segs = [1 + max(0, (int(C[i]) + w - 1) // per - (int(C[i]) + F) // per) if w > 0 else 0
+            for i, w in enumerate(width)]
     return meta, np.concatenate([[0], np.cumsum(segs)]).astype(np.int32)
 
 
@@ -104,8 +100,10 @@ def check_schedule(seqlens, parts, meta, num_splits):
         assert seg_k[i] == list(range(len(seg_k[i]))), f"sequence {i}: split ids {seg_k[i]}"
         assert num_splits[i + 1] - num_splits[i] == len(seg_k[i])
     assert num_splits[0] == 0
-    total = sum(n + SEGMENT_COST for n in pages if n > 0) + SEGMENT_COST * (parts - 1)
+    total = sum(n + SEGMENT_COST for n in pages if n > 0)
     per = max(-(-total // parts), SEGMENT_COST + MIN_PART_PAGES)
+    # a part spans at most `per` units of the cost axis, plus the fixed cost of
+    # a first segment whose start was paid for by the previous part
     assert max(costs, default=0) <= per + SEGMENT_COST, (max(costs), per)
     assert int(num_splits[-1]) <= b + parts
 
