@@ -58,7 +58,8 @@ enum {
   MLA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed                */
   MLA_ERR_BAD_BLOCK_ID = -5, /* device: block_table entry outside the cache      */
   MLA_ERR_TIMEOUT = -6,      /* device: a pipeline wait gave up                  */
-  MLA_ERR_BAD_SEQLEN = -7    /* device: cache_seqlens entry < 0                  */
+  MLA_ERR_BAD_SEQLEN = -7,   /* device: cache_seqlens entry < 0                  */
+  MLA_ERR_SCRATCH_TOO_SMALL = -8 /* the shape needs more than the built-in scratch */
 };
 
 typedef struct CUstream_st *mla_stream_t; /* the same type as cudaStream_t */
@@ -161,6 +162,52 @@ mla_status_t mla_decode_splitkv(const void *q, int b, int s_q, int h_q, int d,
 mla_status_t mla_combine_splits(const int32_t *num_splits, int b, int s_q, int h_q,
                                 const void *workspace, int num_parts, void *out, float *lse,
                                 mla_stream_t stream);
+
+/*
+ * Bytes of the library's built-in split-KV scratch (64 MiB), used by
+ * mla_decode_with_kvcache_static.
+ */
+#define MLA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+
+/*
+ * mla_decode_with_kvcache without the `workspace` arguments: the split-KV
+ * scratch (partial outputs of sequences cut into several pieces) comes from a
+ * buffer of MLA_STATIC_WORKSPACE_BYTES that the library itself holds in device
+ * memory, so the call allocates nothing and needs nothing allocated for it
+ * beyond its inputs and outputs.  The pages have no counterpart of this call.
+ *
+ * It exists for callers that have no way to obtain device memory of their
+ * own at the point of the call: code running while a CUDA stream is being
+ * captured into a graph (where cudaMalloc is not allowed), or code loaded into
+ * a host program whose device memory is entirely owned by that program's pool
+ * and which gives its plug-ins no allocator.
+ *
+ * Limits and behaviour:
+ *  - Every process that loads the library keeps the 64 MiB buffer on each GPU
+ *    where the library's kernels are loaded, until it exits.
+ *  - Shapes whose mla_workspace_bytes(b, s_q, h_q, num_parts) exceeds
+ *    MLA_STATIC_WORKSPACE_BYTES are rejected with MLA_ERR_SCRATCH_TOO_SMALL
+ *    before anything is enqueued (b=128, s_q=1, h_q=128 with 76 parts needs
+ *    about 54 MB and fits).
+ *  - The first call on a device looks the buffer's device address up
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before starting any stream capture.
+ *  - All calls share the one buffer: calls whose kernels may overlap on the
+ *    GPU (different streams without ordering, or several host threads) race
+ *    on it and give undefined results.  Calls ordered on one stream are safe.
+ *    The buffer keeps the last call's contents; nothing in it needs to start
+ *    at zero, because each call writes every scratch entry it later reads.
+ * All other arguments, results and errors are those of mla_decode_with_kvcache.
+ */
+mla_status_t mla_decode_with_kvcache_static(const void *q, int b, int s_q, int h_q, int d,
+                                            const void *kcache, int64_t num_blocks,
+                                            int block_size, int h_kv, int stride,
+                                            const int32_t *block_table, int max_blocks_per_seq,
+                                            const int32_t *cache_seqlens, int dv,
+                                            const int32_t *metadata, int num_parts,
+                                            const int32_t *num_splits, float softmax_scale,
+                                            int causal, void *out, float *lse, int32_t *status,
+                                            mla_stream_t stream);
 
 #ifdef __cplusplus
 }

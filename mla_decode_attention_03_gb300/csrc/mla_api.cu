@@ -77,6 +77,7 @@ const char* mla_status_string(mla_status_t s) {
     case MLA_ERR_BAD_BLOCK_ID: return "MLA_ERR_BAD_BLOCK_ID: block_table entry outside [0, num_blocks)";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a decode pipeline wait gave up";
     case MLA_ERR_BAD_SEQLEN: return "MLA_ERR_BAD_SEQLEN: negative cache_seqlens entry";
+    case MLA_ERR_SCRATCH_TOO_SMALL: return "MLA_ERR_SCRATCH_TOO_SMALL: shape needs more split-KV scratch than the library's built-in 64 MiB";
     default: return "MLA: unknown status";
   }
 }
@@ -268,3 +269,48 @@ mla_status_t mla_combine_splits(const int32_t* num_splits, int b, int s_q, int h
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  The split-KV scratch lives in this file-scope
+// device array instead of a caller-provided workspace.  Host code may not use
+// the array's name as a device address (on the host it only stands for the
+// symbol), so its address is looked up once per device with that device
+// current, and that address is what the kernels receive.
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+mla_status_t static_workspace(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return MLA_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" mla_status_t mla_decode_with_kvcache_static(
+    const void* q, int b, int s_q, int h_q, int d, const void* kcache, int64_t num_blocks, int block_size,
+    int h_kv, int stride, const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
+    int dv, const int32_t* metadata, int num_parts, const int32_t* num_splits, float softmax_scale,
+    int causal, void* out, float* lse, int32_t* status, mla_stream_t stream) {
+  const size_t need = mla_workspace_bytes(b, s_q, h_q, num_parts);
+  if (need == 0) return MLA_ERR_INVALID_ARG;
+  if (need > MLA_STATIC_WORKSPACE_BYTES) return MLA_ERR_SCRATCH_TOO_SMALL;
+  void* ws = nullptr;
+  const mla_status_t r = static_workspace(&ws);
+  if (r != MLA_OK) return r;
+  return decode_impl(q, b, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride, block_table,
+                     max_blocks_per_seq, cache_seqlens, dv, metadata, num_parts, num_splits,
+                     softmax_scale, causal, out, lse, ws, MLA_STATIC_WORKSPACE_BYTES, status, stream, true);
+}

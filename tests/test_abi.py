@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "mla_status_string", "mla_num_parts", "mla_metadata_ints", "mla_workspace_bytes",
-        "mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits"])
+        "mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits",
+        "mla_decode_with_kvcache_static"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -90,6 +91,6 @@ def test_sizes_and_strings(lib):
     assert lib.mla_workspace_bytes(128, 1, 128, 76) == o + ((l + 255) // 256) * 256
     assert lib.mla_workspace_bytes(0, 1, 128, 76) == 0
     assert lib.mla_metadata_ints(76) == 76 * 8
-    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert lib.mla_status_string(code).startswith(b"MLA_")
     assert lib.mla_status_string(12345) == b"MLA: unknown status"
