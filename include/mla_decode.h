@@ -164,6 +164,38 @@ mla_status_t mla_combine_splits(const int32_t *num_splits, int b, int s_q, int h
                                 mla_stream_t stream);
 
 /*
+ * Cache maintenance next to the decode (MLA caches have one latent KV head).
+ *
+ * mla_write_cache puts new tokens into the paged cache the decode reads:
+ * for each token t with s = slot_mapping[t] >= 0, entry
+ * (page s / block_size, slot s % block_size) receives the 512 latent values
+ * kv_c[t] followed by the 64 rope values k_pe[t].  Negative slot ids are
+ * skipped (padding tokens); slot ids >= num_blocks*block_size are skipped
+ * and reported as MLA_ERR_BAD_BLOCK_ID in `status`.  The pad of 640-element
+ * entries is never written.
+ *   kv_c          bf16 rows of 512, `kv_c_row_stride` elements apart (>= 512, multiple of 8)
+ *   k_pe          bf16 rows of 64, `k_pe_row_stride` elements apart (>= 64, multiple of 8)
+ *   slot_mapping  int64[num_tokens]
+ *   kcache        as for mla_decode_with_kvcache with h_kv = 1
+ * All device pointers 16-byte aligned.  One kernel on `stream`.
+ *
+ * mla_copy_blocks is copy_blocks_mla of vLLM PR #12676: for each of
+ * `num_layers` caches (kcaches: a DEVICE array of num_layers device pointers,
+ * each 16-byte aligned) and each pair (src, dst) of block_mapping (int64[num_pairs][2],
+ * device), page dst becomes a copy of page src, pad included.  Sources and
+ * destinations must be disjoint; ids outside [0, num_blocks) are skipped and
+ * reported as MLA_ERR_BAD_BLOCK_ID.  One kernel on `stream`.
+ */
+mla_status_t mla_write_cache(const void *kv_c, int64_t kv_c_row_stride, const void *k_pe,
+                             int64_t k_pe_row_stride, const int64_t *slot_mapping,
+                             int64_t num_tokens, void *kcache, int64_t num_blocks, int block_size,
+                             int stride, int32_t *status, mla_stream_t stream);
+
+mla_status_t mla_copy_blocks(const uint64_t *kcaches, int num_layers, const int64_t *block_mapping,
+                             int64_t num_pairs, int64_t num_blocks, int block_size, int stride,
+                             int32_t *status, mla_stream_t stream);
+
+/*
  * Bytes of the library's built-in split-KV scratch (64 MiB), used by
  * mla_decode_with_kvcache_static.
  */

@@ -246,6 +246,38 @@ mla_status_t mla_decode_splitkv(const void* q, int b, int s_q, int h_q, int d, c
                      softmax_scale, causal, out, lse, workspace, workspace_bytes, status, stream, false);
 }
 
+mla_status_t mla_write_cache(const void* kv_c, int64_t kv_c_row_stride, const void* k_pe, int64_t k_pe_row_stride,
+                             const int64_t* slot_mapping, int64_t num_tokens, void* kcache, int64_t num_blocks,
+                             int block_size, int stride, int32_t* status, mla_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || !kcache || !status) return MLA_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!kv_c || !k_pe || !slot_mapping)) return MLA_ERR_INVALID_ARG;
+  if (block_size != kPage) return MLA_ERR_UNSUPPORTED;
+  if (stride < kDimQK || kv_c_row_stride < kDimV || k_pe_row_stride < kDimQK - kDimV) return MLA_ERR_INVALID_ARG;
+  if (stride % 8 || kv_c_row_stride % 8 || k_pe_row_stride % 8) return MLA_ERR_ALIGNMENT;
+  if ((num_tokens > 0 && (!aligned16(kv_c) || !aligned16(k_pe))) || !aligned16(kcache)) return MLA_ERR_ALIGNMENT;
+  if ((num_tokens + 7) / 8 > 0x7fffffff) return MLA_ERR_INVALID_ARG;
+  return mla::launch_write_cache(kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens, kcache,
+                                 num_blocks * kPage, stride, status, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_copy_blocks(const uint64_t* kcaches, int num_layers, const int64_t* block_mapping,
+                             int64_t num_pairs, int64_t num_blocks, int block_size, int stride, int32_t* status,
+                             mla_stream_t stream) {
+  if (num_layers < 0 || num_layers > 65535 || num_pairs < 0 || num_pairs > 0x7fffffff || num_blocks < 1 || !status)
+    return MLA_ERR_INVALID_ARG;
+  if (num_layers > 0 && num_pairs > 0 && (!kcaches || !block_mapping)) return MLA_ERR_INVALID_ARG;
+  if (block_size != kPage) return MLA_ERR_UNSUPPORTED;
+  if (stride < kDimQK) return MLA_ERR_INVALID_ARG;
+  if (stride % 8) return MLA_ERR_ALIGNMENT;
+  return mla::launch_copy_blocks(kcaches, num_layers, block_mapping, num_pairs, num_blocks, block_size, stride,
+                                 status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
 mla_status_t mla_combine_splits(const int32_t* num_splits, int b, int s_q, int h_q,
                                 const void* workspace, int num_parts, void* out, float* lse,
                                 mla_stream_t stream) {

@@ -61,5 +61,11 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, int32_t* metadata,
                             int32_t* num_splits, int32_t* status, cudaStream_t stream);
 cudaError_t decode_max_active_clusters(int* clusters);
+cudaError_t launch_write_cache(const void* kv_c, int64_t kv_c_row_elems, const void* k_pe, int64_t k_pe_row_elems,
+                               const int64_t* slot_mapping, int64_t num_tokens, void* kcache, int64_t num_slots,
+                               int stride, int32_t* status, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const uint64_t* caches, int num_layers, const int64_t* mapping, int64_t num_pairs,
+                               int64_t num_blocks, int block_size, int stride, int32_t* status,
+                               cudaStream_t stream);
 
 }  // namespace mla

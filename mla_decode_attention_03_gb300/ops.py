@@ -50,6 +50,10 @@ def load_library():
         fn.argtypes = [P, I, I, I, I, P, I64, I, I, I, P, I, P, I, P, I, P, F, I, P, P, P, SZ, P, P]
     lib.mla_combine_splits.restype = ctypes.c_int32
     lib.mla_combine_splits.argtypes = [P, I, I, I, P, I, P, P, P]
+    lib.mla_write_cache.restype = ctypes.c_int32
+    lib.mla_write_cache.argtypes = [P, I64, P, I64, P, I64, P, I64, I, I, P, P]
+    lib.mla_copy_blocks.restype = ctypes.c_int32
+    lib.mla_copy_blocks.argtypes = [P, I, P, I64, I64, I, I, P, P]
     _lib = lib
     return lib
 
@@ -169,6 +173,54 @@ def combine_splits(num_splits: torch.Tensor, workspace: torch.Tensor, parts: int
                                              parts, out.data_ptr(), lse.data_ptr(), _stream_handle()),
            "mla_combine_splits")
     return out, lse
+
+
+def write_cache(kv_c: torch.Tensor, k_pe: torch.Tensor, slot_mapping: torch.Tensor, kcache: torch.Tensor,
+                status: torch.Tensor | None = None):
+    """New tokens into the paged cache: entry slot_mapping[t] <- [kv_c[t], k_pe[t]]
+    (mla_write_cache).  kcache is the [num_blocks, 64, 1, 576] view of the cache."""
+    if kv_c.dtype != torch.bfloat16 or k_pe.dtype != torch.bfloat16 or kcache.dtype != torch.bfloat16:
+        raise MLAError("kv_c, k_pe and kcache must be bfloat16")
+    if kv_c.stride(-1) != 1 or k_pe.stride(-1) != 1:
+        raise MLAError("kv_c and k_pe rows must be contiguous")
+    if kv_c.shape[-1] != 512 or k_pe.shape[-1] != 64 or kv_c.dim() != 2 or k_pe.dim() != 2:
+        raise MLAError("kv_c must be [T, 512] and k_pe [T, 64]")
+    if kv_c.shape[0] != k_pe.shape[0] or slot_mapping.numel() != kv_c.shape[0]:
+        raise MLAError("kv_c, k_pe and slot_mapping must have one row per token")
+    if kv_c.device != kcache.device or k_pe.device != kcache.device:
+        raise MLAError("kv_c, k_pe and kcache must be on one device")
+    sm = slot_mapping.to(device=kcache.device, dtype=torch.int64).contiguous()
+    nb, bs, h_kv, _ = kcache.shape
+    if h_kv != 1:
+        raise MLAError("MLA caches have one latent head")
+    if status is None:
+        status = new_status(kcache.device)
+    _check(load_library().mla_write_cache(kv_c.data_ptr(), kv_c.stride(0), k_pe.data_ptr(), k_pe.stride(0),
+                                          sm.data_ptr(), sm.numel(), kcache.data_ptr(), nb, bs,
+                                          entry_stride(kcache), status.data_ptr(), _stream_handle()),
+           "mla_write_cache")
+    return kcache
+
+
+def copy_blocks(kcaches: list, block_mapping: torch.Tensor, status: torch.Tensor | None = None):
+    """copy_blocks_mla: for every layer cache and (src, dst) pair, page dst <- page src."""
+    if not kcaches:
+        return kcaches
+    nb, bs, h_kv, _ = kcaches[0].shape
+    stride = entry_stride(kcaches[0])
+    for c in kcaches:
+        if c.dtype != torch.bfloat16 or c.device != kcaches[0].device:
+            raise MLAError("layer caches must be bfloat16 tensors on one device")
+        if c.shape != kcaches[0].shape or entry_stride(c) != stride:
+            raise MLAError("all layer caches must share one shape and entry stride")
+    dev = kcaches[0].device
+    ptrs = torch.tensor([c.data_ptr() for c in kcaches], dtype=torch.int64, device=dev)
+    bm = block_mapping.to(device=dev, dtype=torch.int64).contiguous()
+    if status is None:
+        status = new_status(dev)
+    _check(load_library().mla_copy_blocks(ptrs.data_ptr(), len(kcaches), bm.data_ptr(), bm.shape[0], nb, bs,
+                                          stride, status.data_ptr(), _stream_handle()), "mla_copy_blocks")
+    return kcaches
 
 
 class MLADecoder:

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "mla_status_string", "mla_num_parts", "mla_metadata_ints", "mla_workspace_bytes",
         "mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits",
-        "mla_decode_with_kvcache_static"])
+        "mla_decode_with_kvcache_static", "mla_write_cache", "mla_copy_blocks"])
 
 
 def test_every_declared_symbol_is_exported(lib):
