@@ -40,6 +40,24 @@ from mla_decode_attention_03_gb300 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch,
+# taken from one ncu capture, keyed by a digest of the kernel's sources and by
+# the workload (name, entry stride).  A kernel whose sources changed since the
+# capture reports null traffic.
+KERNEL_SOURCES = ("mla_decode.cu", "sm103_ptx.cuh")
+MEASURED_TRAFFIC = {
+    ("0a8a2717d32fc9f2", "bench", 576): 627163136,
+}
+
+
+def kernel_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mla_decode_attention_03_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
 
 def metric_bytes_flops(w) -> tuple[int, int]:
     S = int(w.cache_seqlens.sum())
@@ -92,7 +110,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def window(self, t0: float, t1: float):
+        """Keep only the samples taken between t0 and t1 (perf_counter seconds)."""
+        self.lines = [(t, ln) for t, ln in self.lines if t0 <= t <= t1]
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -105,7 +127,7 @@ class ClockSampler:
     def summary(self):
         mhz, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for _, line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 6:
                 continue
@@ -185,22 +207,25 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[3].record(stream)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    ops.check_status(dec.status)
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
+    # the clock sampler starts before the warm-up so that its own start-up falls
+    # outside the timed loop; only samples taken during the loop are kept
     with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+        torch.cuda.synchronize()
+        ops.check_status(dec.status)
+        barrier(world)
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for k in range(args.steps):
             flush.fill_(k & 0xFF)  # L2 flush: a 512 MB write between steps, outside the events
             step(evs[k])
         torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        wall = t1 - t0
+    clk.window(t0, t1)
     barrier(world)
     ops.check_status(dec.status)
     t_meta = [e[0].elapsed_time(e[1]) for e in evs]
@@ -247,7 +272,8 @@ def run_ours(args, world, rank, local):
                          "decode_median": round(1e3 * float(np.median(t_dec)), 2)},
         "wall_s_timed_loop": round(wall, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": MEASURED_TRAFFIC.get((kernel_digest(), w.name, w.stride)),
                      "kernel": "mla_decode_kernel", "peak_source": peak_src,
                      "tensor_tflops_achieved": round(flops / 1e9 / ms_dec, 1),
                      "tensor_frac": round(flops / 1e9 / ms_dec / tf_peak, 4)},
@@ -395,6 +421,58 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Bandwidth against mean sequence length at b=128, h_q=128 (the shape of the
+    seqlen sweep plotted in the PAI tutorial, section 4), for the 576- and
+    640-element entry layouts.  Inputs are drawn on the device (a seeded
+    torch generator): this mode times only, it compares nothing."""
+    from mla_decode_attention_03_gb300 import ops
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    b, h_q = 128, 128
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    parts = ops.num_parts(1, h_q, 1, dev)
+    dec = ops.MLADecoder(b, 1, h_q, 1, device=dev, parts=parts)
+    q = torch.randn((b, 1, h_q, 576), generator=gen, device=dev).to(torch.bfloat16)
+    for L in [int(x) for x in args.sweep.split(",")]:
+        n_pages = -(-L // 64)
+        for stride in (576, 640):
+            kc_alloc = torch.zeros((b * n_pages, 64, 1, stride), dtype=torch.bfloat16, device=dev)
+            kc_alloc[..., :576] = torch.randn((b * n_pages, 64, 1, 576), generator=gen, device=dev)
+            kc = kc_alloc[..., :576]
+            bt = torch.arange(b * n_pages, dtype=torch.int32, device=dev).view(b, n_pages)
+            sl = torch.full((b,), L, dtype=torch.int32, device=dev)
+            out = torch.empty((b, 1, h_q, 512), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((b, h_q, 1), dtype=torch.float32, device=dev)
+            nbytes = (b * L * 576 + b * h_q * 576 + b * h_q * 512) * 2
+
+            def step():
+                meta, nsplit = ops.get_mla_metadata(sl, parts, dec.status)
+                ops.mla_decode_with_kvcache(q, kc, bt, sl, meta, nsplit, 576 ** -0.5, False, out=out,
+                                            lse=lse, workspace=dec.workspace, status=dec.status)
+            for _ in range(5):
+                flush.fill_(1)
+                step()
+            evs = []
+            for k in range(args.steps):
+                flush.fill_(k & 0xFF)
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                step()
+                e.record()
+                evs.append((a, e))
+            torch.cuda.synchronize()
+            ops.check_status(dec.status)
+            ms = float(np.mean([a.elapsed_time(e) for a, e in evs]))
+            print(json.dumps({"mode": "sweep", "mean_seqlen": L, "stride": stride, "b": b, "h_q": h_q,
+                              "ms": round(ms, 5), "GB/s": round(nbytes / 1e6 / ms, 1),
+                              "TFLOPS": round(2 * b * L * h_q * 1088 / 1e9 / ms, 1)}), flush=True)
+            del kc_alloc, kc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,7 +482,12 @@ def main():
     ap.add_argument("--workload", default="bench", choices=sorted(W.WORKLOADS))
     ap.add_argument("--stride", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated mean sequence lengths: print one line per (length, stride)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
