@@ -14,23 +14,33 @@
 //  * One 2-CTA cluster per scheduler part.  The pair splits the contraction
 //    dimension: CTA r owns latent dims [256r, 256r+256) and rope dims
 //    [512+32r, 512+32r+32).  Each CTA TMA-loads only its 288 dims of every page
-//    (no byte is fetched twice), computes a partial S = Q K^T over them on the
-//    tensor cores, and the two partials are swapped through distributed shared
-//    memory and summed (a+b == b+a bitwise, so both CTAs hold the same S and take
-//    identical softmax decisions).  Each CTA then multiplies P by its own V half
-//    (its latent dims are exactly half of V), so O [128 x 512] fp32 -- which
-//    would fill all of one SM's tensor memory -- is split 256 columns per SM.
+//    (no byte is fetched twice) and computes a partial S = Q K^T over them on the
+//    tensor cores.  The partials are swapped through distributed shared memory
+//    as int16 with one fp32 scale per (row, 32 tokens) -- half the bytes of fp32,
+//    which matters because SM-to-SM bandwidth, not HBM, bounds this exchange.
+//    Each CTA adds its own exact fp32 partial to the dequantised peer partial, so
+//    the two CTAs see scores that differ by at most one quantisation step
+//    (1/32767 of the largest partial of that row and 32 tokens); each CTA runs its own
+//    online softmax and normalises its own output half with its own sums.  Each
+//    CTA multiplies P by its own V half (its latent dims are exactly half of V),
+//    so O [128 x 512] fp32 -- which would fill all of one SM's tensor memory --
+//    is split 256 columns per SM.
 //  * Tensor memory per CTA: O half (256 columns), two S buffers (64 columns
-//    each; P overwrites S in place as packed bf16 and feeds PV straight from
-//    tensor memory), and the CTA's latent half of Q (128 columns, bf16), so
-//    QK reads only K from shared memory.  Shared memory holds 4 K stages, two
-//    exchange slots and the rope quarter of Q.
+//    each), one P buffer (32 columns of packed bf16 that feed PV straight from
+//    tensor memory) and 192 of the CTA's 256 latent Q dims (96 columns); the
+//    other 64 latent Q dims and the rope quarter sit in shared memory.
 //  * Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma and owns
-//    tensor memory, warps 2-5 do the online softmax (one query row per thread)
-//    and the epilogue, warps 6-9 stage each sequence's Q into tensor memory.
-//    All hand-offs are mbarriers; every wait is bounded.
-//  * tcgen05.mma operations of one thread execute in issue order, so QK(n+2)
-//    is issued right behind PV(n) into the buffer PV(n) reads P from.
+//    tensor memory, warps 2-9 do the online softmax and the epilogue (warps w
+//    and w+4 share a tensor-memory lane quadrant and take 32 tokens each of the
+//    same 32 rows), warps 10-13 stage each sequence's Q.
+//  * The softmax loop is skewed by one page: it reads S(n), quantises and sends
+//    its partial, then finishes page n-1 (whose peer partial arrived meanwhile)
+//    while page n's exchange is in flight.  QK runs two pages ahead of PV; an S
+//    buffer is handed back to the MMA warp as soon as it has been read.
+//  * Exchange slots are returned to the sender by an explicit credit (the
+//    receiver's MMA warp arrives on the sender's barrier once P of that page
+//    exists), so no slot is overwritten before it is read.  All hand-offs are
+//    mbarriers; every wait is bounded.
 //  * Scores use exp2 with scale*log2(e) folded in; the running max is only
 //    moved (and O rescaled in tensor memory) when it grows by more than 8, so
 //    rescaling is rare.
@@ -42,44 +52,64 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kStages = 4;
 constexpr int kKChunk = kPage * 128;           // 64 tokens x 64 dims bf16 (128B swizzle)
 constexpr int kKRope = kPage * 64;             // 64 tokens x 32 dims bf16 (64B swizzle)
 constexpr int kKStage = 4 * kKChunk + kKRope;  // 36864 bytes: this CTA's 288 dims of a page
-constexpr int kXSlot = kRowsPerTile * 256;     // exchange: 128 rows x 64 fp32
+constexpr int kXSlots = 2;     // receive slots (peer partials)
+constexpr int kXData = kRowsPerTile * 128;     // 128 rows x 64 int16 (two 32-token halves)
+constexpr int kXSlot = kXData + 2 * kRowsPerTile * 4;  // + one fp32 scale per (row, half)
 constexpr int kQRope = kRowsPerTile * 64;      // Q rope quarter: 128 rows x 32 bf16 (64B swizzle)
+constexpr int kQLat = kRowsPerTile * 128;      // Q latent dims [192, 256) of the CTA: 128 rows x 64 bf16
 
 constexpr int kOffK = 0;
 constexpr int kOffX = kOffK + kStages * kKStage;
-constexpr int kOffQR = kOffX + 2 * kXSlot;
-constexpr int kOffBar = kOffQR + kQRope;
+constexpr int kOffStg = kOffX + kXSlots * kXSlot;
+constexpr int kOffQL = kOffStg + kXSlot;  // 1024-aligned (128B swizzle atom)
+constexpr int kOffQR = kOffQL + kQLat;
+constexpr int kOffRed = kOffQR + kQRope;         // sibling-warp exchange: [3][2 halves][128 rows] fp32
+constexpr int kOffBar = kOffRed + 3 * 2 * kRowsPerTile * 4;
 
 // barrier slots
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + kStages;
 constexpr int kBarQFull = kBarEmpty + kStages;
 constexpr int kBarQEmpty = kBarQFull + 1;
-constexpr int kBarSFull = kBarQEmpty + 1;  // 2
-constexpr int kBarPFull = kBarSFull + 2;   // 2
-constexpr int kBarOFull = kBarPFull + 2;
-constexpr int kBarXFull = kBarOFull + 1;   // 2
-constexpr int kBarDone = kBarXFull + 2;
+constexpr int kBarSFull = kBarQEmpty + 1;   // 2
+constexpr int kBarSFree = kBarSFull + 2;    // 2
+constexpr int kBarPFull = kBarSFree + 2;
+constexpr int kBarOFull = kBarPFull + 1;
+constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
+constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots
+constexpr int kBarXRead = kBarXEmpty + kXSlots;   // kXSlots: softmax warps have read the slot
+constexpr int kBarSib = kBarXRead + kXSlots;  // 4 quadrants x 3 (two page parities + epilogue)
+constexpr int kBarDone = kBarSib + 12;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
+static_assert(kOffQL % 1024 == 0, "Q latent tile must sit on a 128B-swizzle atom");
+static_assert(kOffQR % 512 == 0, "Q rope tile must sit on a 64B-swizzle atom");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;  // S/P buffers: [256, 320), [320, 384)
-constexpr uint32_t kTmemQ = 384;  // Q latent half, bf16 pairs: [384, 512)
+constexpr uint32_t kTmemS = 256;  // S buffers: [256, 320), [320, 384)
+constexpr uint32_t kTmemP = 384;  // P, bf16 pairs: [384, 416)
+constexpr uint32_t kTmemQ = 416;  // Q latent dims [0, 192) of the CTA, bf16 pairs: [416, 512)
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kQuantMax = 32767.0f;
+// q in [-32767, 32767] travels as the low 16 bits of the fp32 value
+// 1.5*2^23 + 32768 + q, whose unit in the last place is 1: one FMA rounds and
+// encodes, one byte permute and one subtraction decode.
+constexpr float kQuantBase = 12615680.0f;  // 1.5 * 2^23 + 32768
+constexpr uint32_t kQuantHi = 0x4B400000u;  // upper half of the bit pattern of 1.5 * 2^23
 
 // --------------------------------------------------------------- schedule
 // A page-by-page walk over the (sequence, page range) segments of one part.
@@ -148,10 +178,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Offset of 16-byte chunk c of exchange row r (XOR swizzle: conflict-free for
-// both the remote writer and the local reader).
+// Offset of 16-byte chunk c (0..7; chunks 4h..4h+3 hold token half h) of
+// exchange row r.  The XOR swizzle makes both the remote writer's and the local
+// reader's accesses conflict-free.
 __device__ __forceinline__ uint32_t x_chunk(int r, int c) {
-  return static_cast<uint32_t>(r * 256 + ((c ^ (r & 15)) << 4));
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t x_scale(int half, int r) {
+  return static_cast<uint32_t>(kXData + (half * kRowsPerTile + r) * 4);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -188,10 +223,16 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarPFull + s), 4);
-      mbar_init(bar(kBarXFull + s), 1);
+      mbar_init(bar(kBarSFree + s), 8);
     }
+    mbar_init(bar(kBarPFull), 8);
     mbar_init(bar(kBarOFull), 1);
+    for (int s = 0; s < kXSlots; ++s) {
+      mbar_init(bar(kBarXFull + s), 1);
+      mbar_init(bar(kBarXEmpty + s), 1);
+      mbar_init(bar(kBarXRead + s), 8);
+    }
+    for (int s = 0; s < 12; ++s) mbar_init(bar(kBarSib + s), 2);
     mbar_init(bar(kBarDone), 1);
     fence_mbar_init();
   }
@@ -199,9 +240,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 6 && rows_valid < kRowsPerTile) {
+  if (warp >= 10 && rows_valid < kRowsPerTile) {
     // Rope rows the Q tile does not fill stay zero (their outputs are discarded).
-    const int t = tid - 192;
+    const int t = tid - 320;
     for (int off = rows_valid * 64 + t * 16; off < kQRope; off += 128 * 16)
       *reinterpret_cast<uint4*>(gbase + kOffQR + off) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -267,27 +308,35 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       // Descriptors are built once; per MMA only a constant offset (>> 4) is added.
       const uint64_t d_klat = smem_desc(base + kOffK, 16, 1024, kSwizzle128B);
       const uint64_t d_krope = smem_desc(base + kOffK + 4 * kKChunk, 16, 512, kSwizzle64B);
+      const uint64_t d_qlat = smem_desc(base + kOffQL, 16, 1024, kSwizzle128B);
       const uint64_t d_qrope = smem_desc(base + kOffQR, 16, 512, kSwizzle64B);
       // V = this CTA's 256 latent dims of the page, read MN-major:
       // 64-dim column blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
       const uint64_t d_v = smem_desc(base + kOffK, kKChunk, 1024, kSwizzle128B);
+      const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
       PageWalk wq, wp;
       wq.start(meta, P.cache_seqlens, P.max_blocks);
       wp = wq;
       int nq = 0, np = 0, qseg = 0;
       bool ok = true;
-      auto issue_qk = [&](const PageWalk& w) -> bool {
-        if (w.first()) {
-          if (!mbar_wait(bar(kBarQFull), qseg & 1, abort_flag)) return false;
-          ++qseg;
-        }
-        const int st = nq % kStages;
-        if (!mbar_wait(bar(kBarFull + st), (nq / kStages) & 1, abort_flag)) return false;
+      // QK(k) needs S buffer k&1 back from the softmax (it has read S(k-2)), the
+      // page's K stage and, on a segment's first page, its Q; PV(k) needs P(k).
+      // Both queues are polled and whichever is ready is issued (QK first), so
+      // a late K load never holds back a PV that is ready.
+      auto qk_ready = [&](const PageWalk& w) -> bool {
+        if (w.first() && !mbar_test(bar(kBarQFull), qseg & 1)) return false;
+        if (nq >= 2 && !mbar_test(bar(kBarSFree + (nq & 1)), ((nq >> 1) - 1) & 1)) return false;
+        return mbar_test(bar(kBarFull + nq % kStages), (nq / kStages) & 1);
+      };
+      auto issue_qk = [&](const PageWalk& w) {
+        if (w.first()) ++qseg;
         tc_fence_after_sync();
-        const uint32_t d = tmem + kTmemS + 64u * (nq & 1);
+        const int sb = nq & 1;
+        const int st = nq % kStages;
+        const uint32_t d = tmem + kTmemS + 64u * sb;
         const uint64_t koff = static_cast<uint64_t>((st * kKStage) >> 4);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 3; ++c) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * ks,
@@ -296,42 +345,58 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           }
         }
 #pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(d, d_qlat + static_cast<uint64_t>((ks * 32) >> 4),
+                    d_klat + koff + static_cast<uint64_t>((3 * kKChunk + ks * 32) >> 4), kIdescQK, 1);
+#pragma unroll
         for (int ks = 0; ks < 2; ++ks)
           umma_bf16(d, d_qrope + static_cast<uint64_t>((ks * 32) >> 4),
                     d_krope + koff + static_cast<uint64_t>((ks * 32) >> 4), kIdescQK, 1);
-        umma_commit(bar(kBarSFull + (nq & 1)));
+        umma_commit(bar(kBarSFull + sb));
         if (w.last()) umma_commit(bar(kBarQEmpty));
         ++nq;
-        return true;
       };
-      auto issue_pv = [&](const PageWalk& w) -> bool {
-        const int pb = np & 1;
-        if (!mbar_wait(bar(kBarPFull + pb), (np >> 1) & 1, abort_flag)) return false;
+      auto issue_pv = [&](const PageWalk& w) {
         tc_fence_after_sync();
         const int st = np % kStages;
         const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
         const uint32_t first = w.first() ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + 64u * pb + 8 * ks,
+          umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
                        d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
                        (first && ks == 0) ? 0u : 1u);
         umma_commit(bar(kBarEmpty + st));
         umma_commit(bar(kBarOFull));
         ++np;
-        return true;
       };
-      // QK runs two pages ahead of PV: one S buffer per page in flight.
-      for (int a = 0; a < 2 && ok && wq.valid; ++a) {
-        ok = issue_qk(wq);
-        wq.advance();
-      }
-      while (ok && wp.valid) {
-        ok = issue_pv(wp);
-        wp.advance();
-        if (ok && wq.valid) {
-          ok = issue_qk(wq);  // into the buffer PV just read P from (in-order execution)
+      // Exchange slots go back to the peer as soon as every softmax warp has
+      // read them; nx counts the pages whose slot has been returned.
+      int nx = 0;
+      long long t_last = clock64();
+      while (wq.valid || wp.valid) {
+        bool issued = false;
+        if (nx < nq && mbar_test(bar(kBarXRead + nx % kXSlots), (nx / kXSlots) & 1)) {
+          mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nx % kXSlots));
+          ++nx;
+          issued = true;
+        }
+        if (issued) {
+        } else if (wq.valid && qk_ready(wq)) {
+          issue_qk(wq);
           wq.advance();
+          issued = true;
+        } else if (wp.valid && np < nq && mbar_test(bar(kBarPFull), np & 1)) {
+          issue_pv(wp);
+          wp.advance();
+          issued = true;
+        }
+        if (issued) {
+          t_last = clock64();
+        } else if (*abort_flag || clock64() - t_last > kWaitTimeoutCycles) {
+          *abort_flag = 1;
+          ok = false;
+          break;
         }
       }
       if (!ok) raise_status(P.status, kStatusTimeout);
@@ -339,15 +404,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       drain_wait(bar(kBarDone), 0);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ================================================= softmax + epilogue
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;  // token half [32*half, 32*half+32) of every page
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const bool leader = (tid == 64);
-    const uint32_t peer_x = cluster_map(base + kOffX, peer);
-    const uint32_t peer_x_full0 = cluster_map(bar(kBarXFull), peer);
-    const uint32_t peer_x_full1 = cluster_map(bar(kBarXFull + 1), peer);
+    float* const red = reinterpret_cast<float*>(gbase + kOffRed);  // [3][2][128]
 
     // row -> (query position, head)
     const int jj = row / P.heads_per_kv;
@@ -359,173 +423,272 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int row_in_seq = j * P.h_q + h;
     const float c_log2 = P.scale_log2;
 
-    PageWalk w;
-    w.start(meta, P.cache_seqlens, P.max_blocks);
+    // wa walks the page being sent (n), wb the page being finished (n - 1).
+    PageWalk wa, wb;
+    wa.start(meta, P.cache_seqlens, P.max_blocks);
+    wb.valid = false;
     float m_run = -INFINITY, l_run = 0.f;
+    int lim_a = 0, lim_b = 0, nseg_epi = 0;
     int n = 0;
     bool ok = true;
-    int lim = 0;
-    while (w.valid && ok) {
-      if (w.first()) {
-        const int L = __ldg(P.cache_seqlens + w.i);
-        lim = P.causal ? L - P.s_q + j + 1 : L;
-        lim = min(lim, L);
-        m_run = -INFINITY;
-        l_run = 0.f;
+    // st.async of the staged page: pieces 0-3 are 16-byte chunks, piece 4 the scale
+    int to_send = 5, send_slot = 0;
+    const uint32_t peer_x = cluster_map(base + kOffX, peer);
+    const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
+    auto send_piece = [&]() {
+      if (to_send >= 5) return;
+      const uint32_t dst = peer_x + static_cast<uint32_t>(send_slot * kXSlot);
+      const uint32_t xb = peer_xfull + 8u * static_cast<uint32_t>(send_slot);
+      const uint8_t* sp = gbase + kOffStg;
+      if (to_send < 4) {
+        const uint32_t off = x_chunk(row, 4 * half + to_send);
+        const uint4 v = *reinterpret_cast<const uint4*>(sp + off);
+        st_async_v4(dst + off, v.x, v.y, v.z, v.w, xb);
+      } else {
+        const uint32_t off = x_scale(half, row);
+        st_async_b32(dst + off, *reinterpret_cast<const uint32_t*>(sp + off), xb);
       }
-      const int sb = n & 1;
-      const uint32_t par = (n >> 1) & 1;
-      if (leader) mbar_arrive_expect_tx(bar(kBarXFull + sb), kXSlot);
-
-      // ---- own partial scores out of tensor memory
-      uint32_t s0[32], s1[32];
-      ok = mbar_wait(bar(kBarSFull + sb), par, abort_flag);
-      if (!ok) break;
-      tc_fence_after_sync();
-      const uint32_t t_s = tmem + lane_off + kTmemS + 64u * sb;
-      tmem_ld32(t_s, s0);
-      tmem_ld32(t_s + 32, s1);
-      tmem_wait_ld2(s0, s1);
-
-      // ---- send them to the peer CTA, take the peer's
-      {
-        const uint32_t dst = peer_x + sb * kXSlot;
-        const uint32_t xb = sb ? peer_x_full1 : peer_x_full0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(dst + x_chunk(row, c), s0[4 * c], s0[4 * c + 1], s0[4 * c + 2], s0[4 * c + 3], xb);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(dst + x_chunk(row, 8 + c), s1[4 * c], s1[4 * c + 1], s1[4 * c + 2], s1[4 * c + 3], xb);
-      }
-      ok = mbar_wait(bar(kBarXFull + sb), par, abort_flag);
-      if (!ok) break;
-      float x[64];
-      {
-        const uint8_t* xr = gbase + kOffX + sb * kXSlot;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 v = *reinterpret_cast<const float4*>(xr + x_chunk(row, c));
-          const uint32_t* src = (c < 8) ? &s0[4 * c] : &s1[4 * (c - 8)];
-          x[4 * c + 0] = (__uint_as_float(src[0]) + v.x) * c_log2;
-          x[4 * c + 1] = (__uint_as_float(src[1]) + v.y) * c_log2;
-          x[4 * c + 2] = (__uint_as_float(src[2]) + v.z) * c_log2;
-          x[4 * c + 3] = (__uint_as_float(src[3]) + v.w) * c_log2;
+      ++to_send;
+    };
+    float a_prev[32];
+    while (ok && (wa.valid || wb.valid)) {
+      float a_cur[32];
+      if (wa.valid) {
+        // ======== page n: own partial out of tensor memory, quantise, send
+        if (wa.first()) {
+          const int L = __ldg(P.cache_seqlens + wa.i);
+          lim_a = min(P.causal ? L - P.s_q + j + 1 : L, L);
         }
-      }
-
-      // ---- online softmax for this row and page
-      const int t0 = w.p * kPage;
-      if (t0 + kPage > lim) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (t0 + c >= lim) x[c] = -INFINITY;
-      }
-      float mx8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = x[u];
-#pragma unroll
-      for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_run, mx);
-      float alpha = 1.f;
-      if (m_new > m_run + kRescaleThreshold) {
-        alpha = ex2_approx(m_run - m_new);  // 0 when m_run = -inf
-        m_run = m_new;
-      }
-      const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
-      const bool rescale_o = !w.first() && alpha != 1.f;
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        // O must hold every earlier page before it is scaled.
-        ok = mbar_wait(bar(kBarOFull), (n - 1) & 1, abort_flag);
+        const int sb = n & 1;
+        const int slot = n % kXSlots;
+        if (leader) mbar_arrive_expect_tx(bar(kBarXFull + slot), kXSlot);
+        ok = mbar_wait(bar(kBarSFull + sb), (n >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kTmemO + 32 * c, o);
-          tmem_wait_ld(o);
+        {
+          uint32_t s[32];
+          tmem_ld32(tmem + lane_off + kTmemS + 64u * sb + 32u * half, s);
+          tmem_wait_ld(s);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tmem + lane_off + kTmemO + 32 * c, o);
+          for (int c = 0; c < 32; ++c) a_cur[c] = __uint_as_float(s[c]);
         }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSFree + sb));
+
+        const int t0 = wa.p * kPage + 32 * half;
+        if (t0 + 32 > lim_a) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (t0 + c >= lim_a) a_cur[c] = 0.f;
+        }
+        float amax8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) amax8[u] = fabsf(a_cur[u]);
+#pragma unroll
+        for (int c = 8; c < 32; ++c) amax8[c & 7] = fmaxf(amax8[c & 7], fabsf(a_cur[c]));
+        const float amax = fmaxf(fmaxf(fmaxf(amax8[0], amax8[1]), fmaxf(amax8[2], amax8[3])),
+                                 fmaxf(fmaxf(amax8[4], amax8[5]), fmaxf(amax8[6], amax8[7])));
+        const float inv = (amax > 0.f) ? __fdividef(kQuantMax, amax) : 0.f;
+        // Stage the encoded partial in this thread's own corner of the staging
+        // slot; it goes out with st.async in pieces while page n-1 is finished.
+        uint8_t* const sp = gbase + kOffStg;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * k + 2 * e;
+            const uint32_t b0 = __float_as_uint(fmaf(a_cur[c], inv, kQuantBase));
+            const uint32_t b1 = __float_as_uint(fmaf(a_cur[c + 1], inv, kQuantBase));
+            wv[e] = __byte_perm(b0, b1, 0x5410);
+          }
+          *reinterpret_cast<uint4*>(sp + x_chunk(row, 4 * half + k)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        *reinterpret_cast<float*>(sp + x_scale(half, row)) = amax * (1.0f / kQuantMax);
+        to_send = 0;
+        send_slot = slot;
       }
 
-      // ---- P (bf16 pairs) over S in tensor memory
-      uint32_t pk[32];
-      float sum8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float e0 = ex2_approx(x[2 * c] - m_sub);
-        const float e1 = ex2_approx(x[2 * c + 1] - m_sub);
-        sum8[c & 7] += e0 + e1;
-        pk[c] = pack_bf16x2(e0, e1);
-      }
-      tmem_st32(t_s, pk);
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
-      const float rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      l_run = l_run * alpha + rsum;
-
-      // ---- epilogue at the end of a segment
-      if (w.last()) {
-        ok = mbar_wait(bar(kBarOFull), n & 1, abort_flag);
+      if (to_send == 0 && n >= kXSlots) {
+        // the peer has read page n - 2 out of the slot page n goes to
+        ok = mbar_wait<true>(bar(kBarXEmpty + send_slot), ((n / kXSlots) - 1) & 1, abort_flag);
         if (!ok) break;
-        tc_fence_after_sync();
-        const int nsplit = __ldg(P.num_splits + w.i + 1) - __ldg(P.num_splits + w.i);
-        const bool direct = (nsplit == 1);
-        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-        const int64_t slot = static_cast<int64_t>(__ldg(P.num_splits + w.i)) + w.k;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kTmemO + 32 * c, o);
-          tmem_wait_ld(o);
-          if (row_live) {
-            const int col = 256 * static_cast<int>(rank) + 32 * c;
-            if (direct) {
-              uint4* dst = reinterpret_cast<uint4*>(
-                  static_cast<__nv_bfloat16*>(P.out) +
-                  ((static_cast<int64_t>(w.i) * rows_total + row_in_seq) * kDimV + col));
+      }
+      if (wb.valid) {
+        // ======== page n - 1: add the peer's partial, online softmax, P
+        const int nb = n - 1;
+        const int slot = nb % kXSlots;
+        if (wb.first()) {
+          m_run = -INFINITY;
+          l_run = 0.f;
+        }
+        ok = mbar_wait(bar(kBarXFull + slot), (nb / kXSlots) & 1, abort_flag);
+        if (!ok) break;
+        float x[32];
+        {
+          const uint8_t* xr = gbase + kOffX + slot * kXSlot;
+          const float sc = *reinterpret_cast<const float*>(xr + x_scale(half, row));
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-                v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-                v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-                v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-                dst[q] = v;
-              }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(
-                  P.ws_o + ((slot * rows_total + row_in_seq) * kDimV + col));
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xr + x_chunk(row, 4 * half + k));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                     __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+            for (int e = 0; e < 4; ++e) {
+              const int c = 8 * k + 2 * e;
+              const float q0 = __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7610)) - kQuantBase;
+              const float q1 = __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7632)) - kQuantBase;
+              x[c] = fmaf(q0, sc, a_prev[c]) * c_log2;
+              x[c + 1] = fmaf(q1, sc, a_prev[c + 1]) * c_log2;
             }
           }
         }
-        if (row_live && rank == 0) {
-          if (direct)
-            P.lse[(static_cast<int64_t>(w.i) * P.h_q + h) * P.s_q + j] = lse;
-          else
-            P.ws_lse[slot * rows_total + row_in_seq] = lse;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarXRead + slot));
+        send_piece();
+        const int t0 = wb.p * kPage + 32 * half;
+        if (t0 + 32 > lim_b) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (t0 + c >= lim_b) x[c] = -INFINITY;
         }
+        float mx8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = x[u];
+#pragma unroll
+        for (int c = 8; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // the sibling warp holds the other 32 tokens of these rows
+        {
+          const int pb = nb & 1;
+          red[(pb * 2 + half) * kRowsPerTile + row] = mx;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarSib + 3 * quad + pb));
+          ok = mbar_wait(bar(kBarSib + 3 * quad + pb), (nb >> 1) & 1, abort_flag);
+          if (!ok) break;
+          mx = fmaxf(mx, red[(pb * 2 + (half ^ 1)) * kRowsPerTile + row]);
+        }
+        send_piece();
+        const float m_new = fmaxf(m_run, mx);
+        float alpha = 1.f;
+        if (m_new > m_run + kRescaleThreshold) {
+          alpha = ex2_approx(m_run - m_new);  // 0 when m_run = -inf
+          m_run = m_new;
+        }
+        const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+        uint32_t pk[16];
+        float sum8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float e0 = ex2_approx(x[2 * c] - m_sub);
+          const float e1 = ex2_approx(x[2 * c + 1] - m_sub);
+          sum8[c & 7] += e0 + e1;
+          pk[c] = pack_bf16x2(e0, e1);
+        }
+        send_piece();
+        const float rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        l_run = l_run * alpha + rsum;
+        // PV of the previous page has to be complete: it read the P buffer, and O
+        // is rescaled below.
+        if (nb >= 1) {
+          ok = mbar_wait(bar(kBarOFull), (nb - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
+        tmem_st16(tmem + lane_off + kTmemP + 16u * half, pk);
+        const bool rescale_o = !wb.first() && alpha != 1.f;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[16];
+            const uint32_t t_o = tmem + lane_off + kTmemO + 128u * half + 16u * c;
+            tmem_ld16(t_o, o);
+            tmem_wait_ld16(o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(t_o, o);
+          }
+        }
+        tmem_wait_st();
         tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPFull));
+        send_piece();
+
+        // ---- epilogue at the end of a segment
+        if (wb.last()) {
+          red[(4 + half) * kRowsPerTile + row] = l_run;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarSib + 3 * quad + 2));
+          ok = mbar_wait(bar(kBarSib + 3 * quad + 2), nseg_epi & 1, abort_flag);
+          if (!ok) break;
+          ++nseg_epi;
+          const float l_tot = red[4 * kRowsPerTile + row] + red[5 * kRowsPerTile + row];
+          ok = mbar_wait(bar(kBarOFull), nb & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const int nsplit = __ldg(P.num_splits + wb.i + 1) - __ldg(P.num_splits + wb.i);
+          const bool direct = (nsplit == 1);
+          const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+          const float lse = (l_tot > 0.f) ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+          const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + wb.i)) + wb.k;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + kTmemO + 128u * half + 32u * c, o);
+            tmem_wait_ld(o);
+            if (row_live) {
+              const int col = 256 * static_cast<int>(rank) + 128 * half + 32 * c;
+              if (direct) {
+                uint4* dstp = reinterpret_cast<uint4*>(
+                    static_cast<__nv_bfloat16*>(P.out) +
+                    ((static_cast<int64_t>(wb.i) * rows_total + row_in_seq) * kDimV + col));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint4 v;
+                  v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+                  v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+                  v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+                  v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+                  dstp[q] = v;
+                }
+              } else {
+                float4* dstp = reinterpret_cast<float4*>(
+                    P.ws_o + ((oslot * rows_total + row_in_seq) * kDimV + col));
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  dstp[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                        __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+              }
+            }
+          }
+          if (row_live && rank == 0 && half == 0) {
+            if (direct)
+              P.lse[(static_cast<int64_t>(wb.i) * P.h_q + h) * P.s_q + j] = lse;
+            else
+              P.ws_lse[oslot * rows_total + row_in_seq] = lse;
+          }
+          tc_fence_before_sync();
+        }
       }
+
+      while (to_send < 5) send_piece();
+      // shift the skew: page n becomes the page to finish
+#pragma unroll
+      for (int c = 0; c < 32; ++c) a_prev[c] = a_cur[c];
+      wb = wa;
+      lim_b = lim_a;
+      if (wa.valid) wa.advance();
       ++n;
-      w.advance();
     }
     if (!ok) raise_status(P.status, kStatusTimeout);
   } else {
-    // ================================================= Q staging into tensor memory
+    // ================================================= Q staging
+    // This CTA's 256 latent dims of each row: [0, 192) into tensor memory as
+    // bf16 pairs, [192, 256) into shared memory (128B swizzle, K-major).
     const int quad = warp & 3;
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
@@ -540,30 +703,40 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     w.start(meta, P.cache_seqlens, P.max_blocks);
     int seg = 0;
     bool ok = true;
-    while (w.valid && ok) {
-      // this CTA's 256 latent dims of the row, as 128 bf16 pairs
-      uint32_t qr[128];
+    auto load32 = [&](const uint8_t* src, uint32_t (&r)[32]) {
       if (row_live) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(
-            qbase + ((static_cast<int64_t>(w.i) * P.s_q + j) * P.h_q + h) * kDimQK + 256 * rank);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < 8; ++k) {
           const uint4 v = ld_global_nc_v4(src + 16 * k);
-          qr[4 * k + 0] = v.x;
-          qr[4 * k + 1] = v.y;
-          qr[4 * k + 2] = v.z;
-          qr[4 * k + 3] = v.w;
+          r[4 * k + 0] = v.x;
+          r[4 * k + 1] = v.y;
+          r[4 * k + 2] = v.z;
+          r[4 * k + 3] = v.w;
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 128; ++k) qr[k] = 0u;
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
       }
+    };
+    while (w.valid && ok) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(
+          qbase + ((static_cast<int64_t>(w.i) * P.s_q + j) * P.h_q + h) * kDimQK + 256 * rank);
+      uint32_t q0[32], q1[32];
+      load32(src, q0);
+      load32(src + 128, q1);
       ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
+      tmem_st32(tmem + lane_off + kTmemQ, q0);
+      tmem_st32(tmem + lane_off + kTmemQ + 32, q1);
+      load32(src + 256, q0);
+      tmem_st32(tmem + lane_off + kTmemQ + 64, q0);
+      load32(src + 384, q1);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tmem_st32(tmem + lane_off + kTmemQ + 32 * k, *reinterpret_cast<const uint32_t(*)[32]>(qr + 32 * k));
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(gbase + kOffQL + row * 128 + ((k ^ (row & 7)) << 4)) =
+            make_uint4(q1[4 * k], q1[4 * k + 1], q1[4 * k + 2], q1[4 * k + 3]);
+      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
