@@ -52,8 +52,9 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr int kStages = 4;
+constexpr int kPrefetchPages = 4;  // pages pulled into L2 ahead of their TMA load
 constexpr int kKChunk = kPage * 128;           // 64 tokens x 64 dims bf16 (128B swizzle)
 constexpr int kKRope = kPage * 64;             // 64 tokens x 32 dims bf16 (64B swizzle)
 constexpr int kKStage = 4 * kKChunk + kKRope;  // 36864 bytes: this CTA's 288 dims of a page
@@ -220,7 +221,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarEmpty + s), 1);
     }
     mbar_init(bar(kBarQFull), 1 + 4);  // rope TMA + the 4 Q-staging warps
-    mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarQEmpty), 2);  // both QK issuers
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarSFree + s), 8);
@@ -233,14 +234,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarXRead + s), 8);
     }
     for (int s = 0; s < 12; ++s) mbar_init(bar(kBarSib + s), 2);
-    mbar_init(bar(kBarDone), 1);
+    mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 10 && rows_valid < kRowsPerTile) {
+  if (warp >= 10 && warp < 14 && rows_valid < kRowsPerTile) {
     // Rope rows the Q tile does not fill stay zero (their outputs are discarded).
     const int t = tid - 320;
     for (int off = rows_valid * 64 + t * 16; off < kQRope; off += 128 * 16)
@@ -261,11 +262,26 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       const uint64_t evict_first = l2_policy_evict_first();
       const int dim_lat = 256 * static_cast<int>(rank);
       const int dim_rope = 512 + 32 * static_cast<int>(rank);
-      PageWalk w;
+      PageWalk w, wpf;
       w.start(meta, P.cache_seqlens, P.max_blocks);
+      wpf = w;
+      // L2 prefetch runs kPrefetchPages ahead of the loads, which then hit L2:
+      // that shortens the load latency the stage ring has to cover.
+      auto prefetch_next = [&]() {
+        if (!wpf.valid) return;
+        const int ph = __ldg(P.block_table + static_cast<int64_t>(wpf.i) * P.max_blocks + wpf.p);
+        if (ph >= 0 && ph < P.num_blocks) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&k_lat, dim_lat + 64 * c, g, ph * kPage);
+          tma_prefetch_l2_3d(&k_rope, dim_rope, g, ph * kPage);
+        }
+        wpf.advance();
+      };
+      for (int a = 0; a < kPrefetchPages; ++a) prefetch_next();
       int n = 0, seg = 0;
       bool ok = true;
       while (w.valid && ok) {
+        prefetch_next();
         if (w.first()) {
           ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
           if (!ok) break;
@@ -303,93 +319,47 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ================================================= MMA issuer
+    // ================================================= PV issuer
+    // Warp 1 issues PV and returns exchange slots to the peer; QK is issued by
+    // warps 14 and 15 (even and odd pages).  Splitting the tcgen05.mma issue
+    // over three sub-partitions keeps any one of them from starving the two
+    // softmax warps it hosts.
     if (lane == 0) {
-      // Descriptors are built once; per MMA only a constant offset (>> 4) is added.
-      const uint64_t d_klat = smem_desc(base + kOffK, 16, 1024, kSwizzle128B);
-      const uint64_t d_krope = smem_desc(base + kOffK + 4 * kKChunk, 16, 512, kSwizzle64B);
-      const uint64_t d_qlat = smem_desc(base + kOffQL, 16, 1024, kSwizzle128B);
-      const uint64_t d_qrope = smem_desc(base + kOffQR, 16, 512, kSwizzle64B);
       // V = this CTA's 256 latent dims of the page, read MN-major:
       // 64-dim column blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
       const uint64_t d_v = smem_desc(base + kOffK, kKChunk, 1024, kSwizzle128B);
       const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
-      PageWalk wq, wp;
-      wq.start(meta, P.cache_seqlens, P.max_blocks);
-      wp = wq;
-      int nq = 0, np = 0, qseg = 0;
+      PageWalk wp;
+      wp.start(meta, P.cache_seqlens, P.max_blocks);
+      int np = 0, nx = 0;
       bool ok = true;
-      // QK(k) needs S buffer k&1 back from the softmax (it has read S(k-2)), the
-      // page's K stage and, on a segment's first page, its Q; PV(k) needs P(k).
-      // Both queues are polled and whichever is ready is issued (QK first), so
-      // a late K load never holds back a PV that is ready.
-      auto qk_ready = [&](const PageWalk& w) -> bool {
-        if (w.first() && !mbar_test(bar(kBarQFull), qseg & 1)) return false;
-        if (nq >= 2 && !mbar_test(bar(kBarSFree + (nq & 1)), ((nq >> 1) - 1) & 1)) return false;
-        return mbar_test(bar(kBarFull + nq % kStages), (nq / kStages) & 1);
-      };
-      auto issue_qk = [&](const PageWalk& w) {
-        if (w.first()) ++qseg;
-        tc_fence_after_sync();
-        const int sb = nq & 1;
-        const int st = nq % kStages;
-        const uint32_t d = tmem + kTmemS + 64u * sb;
-        const uint64_t koff = static_cast<uint64_t>((st * kKStage) >> 4);
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * ks,
-                         d_klat + koff + static_cast<uint64_t>((c * kKChunk + ks * 32) >> 4), kIdescQK,
-                         (c | ks) != 0);
-          }
-        }
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(d, d_qlat + static_cast<uint64_t>((ks * 32) >> 4),
-                    d_klat + koff + static_cast<uint64_t>((3 * kKChunk + ks * 32) >> 4), kIdescQK, 1);
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          umma_bf16(d, d_qrope + static_cast<uint64_t>((ks * 32) >> 4),
-                    d_krope + koff + static_cast<uint64_t>((ks * 32) >> 4), kIdescQK, 1);
-        umma_commit(bar(kBarSFull + sb));
-        if (w.last()) umma_commit(bar(kBarQEmpty));
-        ++nq;
-      };
-      auto issue_pv = [&](const PageWalk& w) {
-        tc_fence_after_sync();
-        const int st = np % kStages;
-        const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
-        const uint32_t first = w.first() ? 1u : 0u;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
-                       d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
-                       (first && ks == 0) ? 0u : 1u);
-        umma_commit(bar(kBarEmpty + st));
-        umma_commit(bar(kBarOFull));
-        ++np;
-      };
-      // Exchange slots go back to the peer as soon as every softmax warp has
-      // read them; nx counts the pages whose slot has been returned.
-      int nx = 0;
       long long t_last = clock64();
-      while (wq.valid || wp.valid) {
-        bool issued = false;
-        if (nx < nq && mbar_test(bar(kBarXRead + nx % kXSlots), (nx / kXSlots) & 1)) {
+      while (wp.valid) {
+        bool issued = true;
+        if (nx <= np && mbar_test(bar(kBarXRead + nx % kXSlots), (nx / kXSlots) & 1)) {
+          // every softmax warp has read the peer's partial of page nx
           mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nx % kXSlots));
           ++nx;
-          issued = true;
-        }
-        if (issued) {
-        } else if (wq.valid && qk_ready(wq)) {
-          issue_qk(wq);
-          wq.advance();
-          issued = true;
-        } else if (wp.valid && np < nq && mbar_test(bar(kBarPFull), np & 1)) {
-          issue_pv(wp);
+        } else if (mbar_test(bar(kBarPFull), np & 1)) {
+          tc_fence_after_sync();
+          const int st = np % kStages;
+          const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
+          const uint32_t first = wp.first() ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
+                         d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
+                         (first && ks == 0) ? 0u : 1u);
+          umma_commit(bar(kBarEmpty + st));
+          umma_commit(bar(kBarOFull));
+          ++np;
           wp.advance();
-          issued = true;
+        } else {
+          issued = false;
+          if (nx <= np)
+            mbar_try_wait_for(bar(kBarXRead + nx % kXSlots), (nx / kXSlots) & 1, 200);
+          else
+            mbar_try_wait_for(bar(kBarPFull), np & 1, 200);
         }
         if (issued) {
           t_last = clock64();
@@ -398,6 +368,80 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           ok = false;
           break;
         }
+      }
+      if (!ok) raise_status(P.status, kStatusTimeout);
+      umma_commit(bar(kBarDone));
+      drain_wait(bar(kBarDone), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 14) {
+    // ================================================= QK issuers
+    // Warp 14 takes the even pages (S buffer 0, K stages 0 and 2), warp 15 the
+    // odd ones.  QK(k) needs S buffer k&1 back from the softmax (it has read
+    // S(k-2)), the page's K stage and its segment's Q.
+    if (lane == 0) {
+      const int parity = warp - 14;
+      const uint64_t d_klat = smem_desc(base + kOffK, 16, 1024, kSwizzle128B);
+      const uint64_t d_krope = smem_desc(base + kOffK + 4 * kKChunk, 16, 512, kSwizzle64B);
+      const uint64_t d_qlat = smem_desc(base + kOffQL, 16, 1024, kSwizzle128B);
+      const uint64_t d_qrope = smem_desc(base + kOffQR, 16, 512, kSwizzle64B);
+      const uint32_t d = tmem + kTmemS + 64u * static_cast<uint32_t>(parity);
+      PageWalk w;
+      w.start(meta, P.cache_seqlens, P.max_blocks);
+      int n = 0, seg = 0;
+      bool ok = true;
+      while (w.valid && ok) {
+        if (w.first()) {
+          // Both issuers wait for every segment's Q, also for a segment they
+          // own no page of: a parity wait on a barrier that may still be a
+          // phase behind would otherwise pass early.
+          ok = mbar_wait(bar(kBarQFull), seg & 1, abort_flag);
+          if (!ok) break;
+          ++seg;
+        }
+        if ((n & 1) == parity) {
+          if (n >= 2) {
+            ok = mbar_wait(bar(kBarSFree + parity), ((n >> 1) - 1) & 1, abort_flag);
+            if (!ok) break;
+          }
+          const int st = n % kStages;
+          ok = mbar_wait(bar(kBarFull + st), (n / kStages) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t koff = static_cast<uint64_t>((st * kKStage) >> 4);
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * ks,
+                           d_klat + koff + static_cast<uint64_t>((c * kKChunk + ks * 32) >> 4), kIdescQK,
+                           (c | ks) != 0);
+            }
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(d, d_qlat + static_cast<uint64_t>((ks * 32) >> 4),
+                      d_klat + koff + static_cast<uint64_t>((3 * kKChunk + ks * 32) >> 4), kIdescQK, 1);
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            umma_bf16(d, d_qrope + static_cast<uint64_t>((ks * 32) >> 4),
+                      d_krope + koff + static_cast<uint64_t>((ks * 32) >> 4), kIdescQK, 1);
+          umma_commit(bar(kBarSFull + parity));
+        }
+        // Q may be replaced once every QK of this segment is done: two arrivals,
+        // one per issuer, or both from the issuer of a single-page segment.  An
+        // issuer that owns no page of a segment does not arrive for it, so no
+        // arrival can ever count towards the wrong segment.
+        if (w.last()) {
+          if (w.p_end - w.p_begin > 1) {
+            umma_commit(bar(kBarQEmpty));
+          } else if ((n & 1) == parity) {
+            umma_commit(bar(kBarQEmpty));
+            umma_commit(bar(kBarQEmpty));
+          }
+        }
+        ++n;
+        w.advance();
       }
       if (!ok) raise_status(P.status, kStatusTimeout);
       umma_commit(bar(kBarDone));
