@@ -120,7 +120,7 @@ mla_status_t mla_get_metadata(const int32_t *cache_seqlens, int b, int num_parts
  *   dv            must be 512
  *   metadata, num_parts, num_splits: from mla_get_metadata on the same
  *                 cache_seqlens (and the same num_parts)
- *   softmax_scale finite (FlashMLA's benchmark uses d**-0.5)
+ *   softmax_scale finite and > 0 (FlashMLA's benchmark uses d**-0.5)
  *   causal        0 or 1; with 1, query j sees tokens t <= L_i - s_q + j
  *   out           bf16[b, s_q, h_q, 512], 16-byte aligned (written)
  *   lse           fp32[b, h_q, s_q], natural log (written)

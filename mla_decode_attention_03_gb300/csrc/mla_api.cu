@@ -145,7 +145,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
       !workspace || !status)
     return MLA_ERR_INVALID_ARG;
   if (b < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || num_blocks < 1 || max_blocks_per_seq < 1 ||
-      num_parts < 1 || (causal != 0 && causal != 1) || !std::isfinite(softmax_scale))
+      num_parts < 1 || (causal != 0 && causal != 1) || !std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
     return MLA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
   if (d != kDimQK || dv != kDimV || block_size != kPage || h_q / h_kv > mla::kRowsPerTile)

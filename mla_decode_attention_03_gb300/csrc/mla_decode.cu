@@ -465,7 +465,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const bool row_live = (row < rows_valid) && (j < P.s_q);
     const int rows_total = P.s_q * P.h_q;
     const int row_in_seq = j * P.h_q + h;
+    // Scores stay in raw units (q.k); scale*log2(e) is applied inside the exp2
+    // argument, and the lazy-rescale threshold is converted to raw units.
     const float c_log2 = P.scale_log2;
+    const float rescale_raw = kRescaleThreshold / c_log2;
 
     // wa walks the page being sent (n), wb the page being finished (n - 1).
     PageWalk wa, wb;
@@ -582,8 +585,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
               const int c = 8 * k + 2 * e;
               const float q0 = __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7610)) - kQuantBase;
               const float q1 = __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7632)) - kQuantBase;
-              x[c] = fmaf(q0, sc, a_prev[c]) * c_log2;
-              x[c + 1] = fmaf(q1, sc, a_prev[c + 1]) * c_log2;
+              x[c] = fmaf(q0, sc, a_prev[c]);
+              x[c + 1] = fmaf(q1, sc, a_prev[c + 1]);
             }
           }
         }
@@ -616,19 +619,19 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         send_piece();
         const float m_new = fmaxf(m_run, mx);
         float alpha = 1.f;
-        if (m_new > m_run + kRescaleThreshold) {
-          alpha = ex2_approx(m_run - m_new);  // 0 when m_run = -inf
+        if (m_new > m_run + rescale_raw) {
+          alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
           m_run = m_new;
         }
-        const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+        const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
         uint32_t pk[16];
         float sum8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float e0 = ex2_approx(x[2 * c] - m_sub);
-          const float e1 = ex2_approx(x[2 * c + 1] - m_sub);
+          const float e0 = ex2_approx(fmaf(x[2 * c], c_log2, neg_mc));
+          const float e1 = ex2_approx(fmaf(x[2 * c + 1], c_log2, neg_mc));
           sum8[c & 7] += e0 + e1;
           pk[c] = pack_bf16x2(e0, e1);
         }
@@ -677,7 +680,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           const int nsplit = __ldg(P.num_splits + wb.i + 1) - __ldg(P.num_splits + wb.i);
           const bool direct = (nsplit == 1);
           const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-          const float lse = (l_tot > 0.f) ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+          const float lse = (l_tot > 0.f) ? (m_run * c_log2 + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
           const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + wb.i)) + wb.k;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {

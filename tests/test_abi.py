@@ -60,7 +60,8 @@ def _decode(lib, **kw):
     (dict(h_q=100, h_kv=3), -1), (dict(b=0), -1), (dict(s_q=0), -1), (dict(stride=500), -1),
     (dict(stride=580), -3), (dict(q=FAKE + 8), -3), (dict(out=FAKE + 2), -3),
     (dict(kcache=FAKE + 4), -3), (dict(workspace_bytes=16), -1), (dict(causal=2), -1),
-    (dict(scale=float("nan")), -1), (dict(num_parts=0), -1), (dict(q=0), -1),
+    (dict(scale=float("nan")), -1), (dict(scale=0.0), -1), (dict(scale=-0.04), -1),
+    (dict(num_parts=0), -1), (dict(q=0), -1),
     (dict(num_blocks=1 << 26), -1),
 ])
 def test_decode_rejects_bad_arguments(lib, kw, code):
