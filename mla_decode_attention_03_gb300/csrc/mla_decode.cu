@@ -179,15 +179,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Offset of 16-byte chunk c (0..7; chunks 4h..4h+3 hold token half h) of
-// exchange row r.  The XOR swizzle makes both the remote writer's and the local
-// reader's accesses conflict-free.
-__device__ __forceinline__ uint32_t x_chunk(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+// Exchange slot layout: softmax thread (warp w, lane l) of one CTA sends its
+// 64 bytes of int16 scores to the thread (w, l) of the peer, which is the only
+// reader.  Chunk k of that thread sits at ((w*4 + k)*32 + l)*16, so each warp
+// instruction writes (and later reads) 512 contiguous bytes; its fp32 scale at
+// kXData + (w*32 + l)*4.
+__device__ __forceinline__ uint32_t x_chunk(int sw, int lane, int k) {
+  return static_cast<uint32_t>(((sw * 4 + k) * 32 + lane) * 16);
 }
 
-__device__ __forceinline__ uint32_t x_scale(int half, int r) {
-  return static_cast<uint32_t>(kXData + (half * kRowsPerTile + r) * 4);
+__device__ __forceinline__ uint32_t x_scale(int sw, int lane) {
+  return static_cast<uint32_t>(kXData + (sw * 32 + lane) * 4);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -452,6 +454,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     // ================================================= softmax + epilogue
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;  // token half [32*half, 32*half+32) of every page
+    const int sw = warp - 2;           // softmax warp index: the exchange slot region it owns
+    const int lane_i = static_cast<int>(lane);
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const bool leader = (tid == 64);
@@ -488,11 +492,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       const uint32_t xb = peer_xfull + 8u * static_cast<uint32_t>(send_slot);
       const uint8_t* sp = gbase + kOffStg;
       if (to_send < 4) {
-        const uint32_t off = x_chunk(row, 4 * half + to_send);
+        const uint32_t off = x_chunk(sw, lane_i, to_send);
         const uint4 v = *reinterpret_cast<const uint4*>(sp + off);
         st_async_v4(dst + off, v.x, v.y, v.z, v.w, xb);
       } else {
-        const uint32_t off = x_scale(half, row);
+        const uint32_t off = x_scale(sw, lane_i);
         st_async_b32(dst + off, *reinterpret_cast<const uint32_t*>(sp + off), xb);
       }
       ++to_send;
@@ -550,9 +554,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
             const uint32_t b1 = __float_as_uint(fmaf(a_cur[c + 1], inv, kQuantBase));
             wv[e] = __byte_perm(b0, b1, 0x5410);
           }
-          *reinterpret_cast<uint4*>(sp + x_chunk(row, 4 * half + k)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(sp + x_chunk(sw, lane_i, k)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
-        *reinterpret_cast<float*>(sp + x_scale(half, row)) = amax * (1.0f / kQuantMax);
+        *reinterpret_cast<float*>(sp + x_scale(sw, lane_i)) = amax * (1.0f / kQuantMax);
         to_send = 0;
         send_slot = slot;
       }
@@ -575,10 +579,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         float x[32];
         {
           const uint8_t* xr = gbase + kOffX + slot * kXSlot;
-          const float sc = *reinterpret_cast<const float*>(xr + x_scale(half, row));
+          const float sc = *reinterpret_cast<const float*>(xr + x_scale(sw, lane_i));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xr + x_chunk(row, 4 * half + k));
+            const uint4 v = *reinterpret_cast<const uint4*>(xr + x_chunk(sw, lane_i, k));
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
