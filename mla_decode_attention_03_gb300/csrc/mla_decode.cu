@@ -84,7 +84,9 @@ constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
 constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots
 constexpr int kBarXRead = kBarXEmpty + kXSlots;   // kXSlots: softmax warps have read the slot
-constexpr int kBarSib = kBarXRead + kXSlots;  // 4 quadrants x 3 (two page parities + epilogue)
+constexpr int kBarStgFull = kBarXRead + kXSlots;  // softmax warps have staged the page
+constexpr int kBarStgFree = kBarStgFull + 1;     // sender warps have read the staging slot
+constexpr int kBarSib = kBarStgFree + 1;  // 4 quadrants x 3 (two page parities + epilogue)
 constexpr int kBarDone = kBarSib + 12;
 constexpr int kNumBars = kBarDone + 1;
 
@@ -235,6 +237,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarXEmpty + s), 1);
       mbar_init(bar(kBarXRead + s), 8);
     }
+    mbar_init(bar(kBarStgFull), 8);
+    mbar_init(bar(kBarStgFree), 4);
     for (int s = 0; s < 12; ++s) mbar_init(bar(kBarSib + s), 2);
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
@@ -482,25 +486,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     int lim_a = 0, lim_b = 0, nseg_epi = 0;
     int n = 0;
     bool ok = true;
-    // st.async of the staged page: pieces 0-3 are 16-byte chunks, piece 4 the scale
-    int to_send = 5, send_slot = 0;
-    const uint32_t peer_x = cluster_map(base + kOffX, peer);
-    const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
-    auto send_piece = [&]() {
-      if (to_send >= 5) return;
-      const uint32_t dst = peer_x + static_cast<uint32_t>(send_slot * kXSlot);
-      const uint32_t xb = peer_xfull + 8u * static_cast<uint32_t>(send_slot);
-      const uint8_t* sp = gbase + kOffStg;
-      if (to_send < 4) {
-        const uint32_t off = x_chunk(sw, lane_i, to_send);
-        const uint4 v = *reinterpret_cast<const uint4*>(sp + off);
-        st_async_v4(dst + off, v.x, v.y, v.z, v.w, xb);
-      } else {
-        const uint32_t off = x_scale(sw, lane_i);
-        st_async_b32(dst + off, *reinterpret_cast<const uint32_t*>(sp + off), xb);
-      }
-      ++to_send;
-    };
     float a_prev[32];
     while (ok && (wa.valid || wb.valid)) {
       float a_cur[32];
@@ -541,8 +526,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         const float amax = fmaxf(fmaxf(fmaxf(amax8[0], amax8[1]), fmaxf(amax8[2], amax8[3])),
                                  fmaxf(fmaxf(amax8[4], amax8[5]), fmaxf(amax8[6], amax8[7])));
         const float inv = (amax > 0.f) ? __fdividef(kQuantMax, amax) : 0.f;
-        // Stage the encoded partial in this thread's own corner of the staging
-        // slot; it goes out with st.async in pieces while page n-1 is finished.
+        // Stage the encoded partial; the sender warps copy it to the peer while
+        // page n-1 is finished here.
+        if (n >= 1) {
+          ok = mbar_wait(bar(kBarStgFree), (n - 1) & 1, abort_flag);
+          if (!ok) break;
+        }
         uint8_t* const sp = gbase + kOffStg;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -557,15 +546,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           *reinterpret_cast<uint4*>(sp + x_chunk(sw, lane_i, k)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
         *reinterpret_cast<float*>(sp + x_scale(sw, lane_i)) = amax * (1.0f / kQuantMax);
-        to_send = 0;
-        send_slot = slot;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarStgFull));
       }
 
-      if (to_send == 0 && n >= kXSlots) {
-        // the peer has read page n - 2 out of the slot page n goes to
-        ok = mbar_wait<true>(bar(kBarXEmpty + send_slot), ((n / kXSlots) - 1) & 1, abort_flag);
-        if (!ok) break;
-      }
       if (wb.valid) {
         // ======== page n - 1: add the peer's partial, online softmax, P
         const int nb = n - 1;
@@ -596,7 +580,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarXRead + slot));
-        send_piece();
         const int t0 = wb.p * kPage + 32 * half;
         if (t0 + 32 > lim_b) {
 #pragma unroll
@@ -620,7 +603,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           if (!ok) break;
           mx = fmaxf(mx, red[(pb * 2 + (half ^ 1)) * kRowsPerTile + row]);
         }
-        send_piece();
         const float m_new = fmaxf(m_run, mx);
         float alpha = 1.f;
         if (m_new > m_run + rescale_raw) {
@@ -639,7 +621,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           sum8[c & 7] += e0 + e1;
           pk[c] = pack_bf16x2(e0, e1);
         }
-        send_piece();
         const float rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l_run = l_run * alpha + rsum;
         // PV of the previous page has to be complete: it read the P buffer, and O
@@ -667,7 +648,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPFull));
-        send_piece();
 
         // ---- epilogue at the end of a segment
         if (wb.last()) {
@@ -726,7 +706,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
       }
 
-      while (to_send < 5) send_piece();
       // shift the skew: page n becomes the page to finish
 #pragma unroll
       for (int c = 0; c < 32; ++c) a_prev[c] = a_cur[c];
@@ -737,9 +716,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     }
     if (!ok) raise_status(P.status, kStatusTimeout);
   } else {
-    // ================================================= Q staging
-    // This CTA's 256 latent dims of each row: [0, 192) into tensor memory as
-    // bf16 pairs, [192, 256) into shared memory (128B swizzle, K-major).
+    // ================================================= Q staging + exchange sending
+    // Warps 10-13 stage each segment's Q -- this CTA's 256 latent dims of each
+    // row: [0, 192) into tensor memory as bf16 pairs, [192, 256) into shared
+    // memory (128B swizzle, K-major) -- and copy every page's staged partial
+    // scores into the peer's receive slot with st.async once the peer has
+    // returned that slot: they, not the softmax warps, absorb the SM-to-SM
+    // link's back-pressure.  A segment's Q is staged as soon as the previous
+    // segment's QKs are done, and at the latest before its first page is sent.
     const int quad = warp & 3;
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
@@ -749,11 +733,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int h = g * P.heads_per_kv + hh;
     const bool row_live = (row < rows_valid) && (j < P.s_q);
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(P.q);
+    const int st_tid = tid - 320;  // 0..127
+    const uint32_t peer_x = cluster_map(base + kOffX, peer);
+    const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
+    constexpr int kChunks = kXSlot / 16;  // 1088 16-byte chunks per page
+    constexpr int kPerThread = (kChunks + 127) / 128;
 
-    PageWalk w;
-    w.start(meta, P.cache_seqlens, P.max_blocks);
-    int seg = 0;
-    bool ok = true;
     auto load32 = [&](const uint8_t* src, uint32_t (&r)[32]) {
       if (row_live) {
 #pragma unroll
@@ -769,14 +754,18 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         for (int k = 0; k < 32; ++k) r[k] = 0u;
       }
     };
-    while (w.valid && ok) {
+    PageWalk wq, w;
+    wq.start(meta, P.cache_seqlens, P.max_blocks);
+    w = wq;
+    int qseg = 0;  // segments whose Q has been staged
+    bool ok = true;
+    auto stage_q = [&]() -> bool {
       const uint8_t* src = reinterpret_cast<const uint8_t*>(
-          qbase + ((static_cast<int64_t>(w.i) * P.s_q + j) * P.h_q + h) * kDimQK + 256 * rank);
+          qbase + ((static_cast<int64_t>(wq.i) * P.s_q + j) * P.h_q + h) * kDimQK + 256 * rank);
       uint32_t q0[32], q1[32];
       load32(src, q0);
       load32(src + 128, q1);
-      ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
-      if (!ok) break;
+      if (!mbar_wait(bar(kBarQEmpty), (qseg & 1) ^ 1, abort_flag)) return false;
       tc_fence_after_sync();
       tmem_st32(tmem + lane_off + kTmemQ, q0);
       tmem_st32(tmem + lane_off + kTmemQ + 32, q1);
@@ -792,8 +781,48 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarQFull));
-      ++seg;
-      w.next_segment();
+      ++qseg;
+      wq.next_segment();
+      return true;
+    };
+    int n = 0, seg = 0;
+    while (ok && w.valid) {
+      if (w.first() && n > 0) ++seg;
+      // this page's segment needs its Q before its page can be staged
+      while (ok && wq.valid && qseg <= seg) ok = stage_q();
+      if (!ok) break;
+      // the next segment's Q, as soon as its slot is free
+      if (wq.valid && qseg == seg + 1 && mbar_test(bar(kBarQEmpty), (qseg & 1) ^ 1)) {
+        ok = stage_q();
+        if (!ok) break;
+      }
+      // ---- send page n
+      ok = mbar_wait(bar(kBarStgFull), n & 1, abort_flag);
+      if (!ok) break;
+      uint4 v[kPerThread];
+      const uint8_t* sp = gbase + kOffStg;
+#pragma unroll
+      for (int k = 0; k < kPerThread; ++k) {
+        const int c = st_tid + 128 * k;
+        if (c < kChunks) v[k] = *reinterpret_cast<const uint4*>(sp + 16 * c);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarStgFree));
+      const int slot = n % kXSlots;
+      if (n >= kXSlots) {
+        // the peer has read page n - 2 out of the slot page n goes to
+        ok = mbar_wait<true>(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, abort_flag);
+        if (!ok) break;
+      }
+      const uint32_t dst = peer_x + static_cast<uint32_t>(slot * kXSlot);
+      const uint32_t xb = peer_xfull + 8u * static_cast<uint32_t>(slot);
+#pragma unroll
+      for (int k = 0; k < kPerThread; ++k) {
+        const int c = st_tid + 128 * k;
+        if (c < kChunks) st_async_v4(dst + 16u * static_cast<uint32_t>(c), v[k].x, v[k].y, v[k].z, v[k].w, xb);
+      }
+      ++n;
+      w.advance();
     }
     if (!ok) raise_status(P.status, kStatusTimeout);
   }

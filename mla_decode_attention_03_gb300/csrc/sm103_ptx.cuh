@@ -113,12 +113,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // at their next poll, so no CTA can spin forever.
 constexpr long long kWaitTimeoutCycles = 4000000000LL;  // about 2 s at 2 GHz
 
+// Cluster-scope acquire variant of mbar_try_wait_for.
+__device__ __forceinline__ bool mbar_try_wait_cluster_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Each poll suspends the thread for up to kWaitSuspendNs (it resumes as soon
+// as the phase completes), so a waiting warp takes almost no issue slots from
+// the warps it shares a sub-partition with.
+constexpr uint32_t kWaitSuspendNs = 20000;
+
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (kCluster ? mbar_try_wait_cluster_for(bar, parity, kWaitSuspendNs)
+                 : mbar_try_wait_for(bar, parity, kWaitSuspendNs))
+      return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitTimeoutCycles) {
       *abort_flag = 1;
