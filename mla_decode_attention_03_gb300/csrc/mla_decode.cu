@@ -526,6 +526,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         const float amax = fmaxf(fmaxf(fmaxf(amax8[0], amax8[1]), fmaxf(amax8[2], amax8[3])),
                                  fmaxf(fmaxf(amax8[4], amax8[5]), fmaxf(amax8[6], amax8[7])));
         const float inv = (amax > 0.f) ? __fdividef(kQuantMax, amax) : 0.f;
+        const uint64_t inv2 = f2(inv, inv), base2 = f2(kQuantBase, kQuantBase);
         // Stage the encoded partial; the sender warps copy it to the peer while
         // page n-1 is finished here.
         if (n >= 1) {
@@ -539,9 +540,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = 8 * k + 2 * e;
-            const uint32_t b0 = __float_as_uint(fmaf(a_cur[c], inv, kQuantBase));
-            const uint32_t b1 = __float_as_uint(fmaf(a_cur[c + 1], inv, kQuantBase));
-            wv[e] = __byte_perm(b0, b1, 0x5410);
+            float t0f, t1f;
+            f2_split(f2_fma(f2(a_cur[c], a_cur[c + 1]), inv2, base2), t0f, t1f);
+            wv[e] = __byte_perm(__float_as_uint(t0f), __float_as_uint(t1f), 0x5410);
           }
           *reinterpret_cast<uint4*>(sp + x_chunk(sw, lane_i, k)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
@@ -564,6 +565,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         {
           const uint8_t* xr = gbase + kOffX + slot * kXSlot;
           const float sc = *reinterpret_cast<const float*>(xr + x_scale(sw, lane_i));
+          const uint64_t sc2 = f2(sc, sc), nbase2 = f2(-kQuantBase, -kQuantBase);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint4 v = *reinterpret_cast<const uint4*>(xr + x_chunk(sw, lane_i, k));
@@ -571,10 +573,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c = 8 * k + 2 * e;
-              const float q0 = __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7610)) - kQuantBase;
-              const float q1 = __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7632)) - kQuantBase;
-              x[c] = fmaf(q0, sc, a_prev[c]);
-              x[c + 1] = fmaf(q1, sc, a_prev[c + 1]);
+              const uint64_t q = f2_add(f2(__uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7610)),
+                                           __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7632))),
+                                        nbase2);
+              f2_split(f2_fma(q, sc2, f2(a_prev[c], a_prev[c + 1])), x[c], x[c + 1]);
             }
           }
         }
@@ -611,16 +613,22 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
         const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
         uint32_t pk[16];
-        float sum8[8];
+        uint64_t sum2[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
+        for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
+        const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float e0 = ex2_approx(fmaf(x[2 * c], c_log2, neg_mc));
-          const float e1 = ex2_approx(fmaf(x[2 * c + 1], c_log2, neg_mc));
-          sum8[c & 7] += e0 + e1;
+          float a0, a1;
+          f2_split(f2_fma(f2(x[2 * c], x[2 * c + 1]), c2, nmc2), a0, a1);
+          const float e0 = ex2_approx(a0);
+          const float e1 = ex2_approx(a1);
+          sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
           pk[c] = pack_bf16x2(e0, e1);
         }
+        float sum8[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f2_split(sum2[u], sum8[2 * u], sum8[2 * u + 1]);
         const float rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l_run = l_run * alpha + rsum;
         // PV of the previous page has to be complete: it read the P buffer, and O
