@@ -595,36 +595,42 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         for (int c = 8; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
         float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // the sibling warp holds the other 32 tokens of these rows
-        {
-          const int pb = nb & 1;
-          red[(pb * 2 + half) * kRowsPerTile + row] = mx;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarSib + 3 * quad + pb));
-          ok = mbar_wait(bar(kBarSib + 3 * quad + pb), (nb >> 1) & 1, abort_flag);
-          if (!ok) break;
-          mx = fmaxf(mx, red[(pb * 2 + (half ^ 1)) * kRowsPerTile + row]);
-        }
-        const float m_new = fmaxf(m_run, mx);
+        // The sibling warp holds the other 32 tokens of these rows.  Its max is
+        // posted now and read after P has been computed speculatively with the
+        // running max, which stays in force on almost every page; only when the
+        // page moves the max (and on a segment's first page) is P recomputed.
+        const int pb = nb & 1;
+        red[(pb * 2 + half) * kRowsPerTile + row] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSib + 3 * quad + pb));
         float alpha = 1.f;
-        if (m_new > m_run + rescale_raw) {
-          alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
-          m_run = m_new;
-        }
-        const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
         uint32_t pk[16];
         uint64_t sum2[4];
+        auto compute_p = [&](float neg_mc) {
+          const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
-        const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
+          for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float a0, a1;
-          f2_split(f2_fma(f2(x[2 * c], x[2 * c + 1]), c2, nmc2), a0, a1);
-          const float e0 = ex2_approx(a0);
-          const float e1 = ex2_approx(a1);
-          sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
-          pk[c] = pack_bf16x2(e0, e1);
+          for (int c = 0; c < 16; ++c) {
+            float a0, a1;
+            f2_split(f2_fma(f2(x[2 * c], x[2 * c + 1]), c2, nmc2), a0, a1);
+            const float e0 = ex2_approx(a0);
+            const float e1 = ex2_approx(a1);
+            sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+        };
+        compute_p((m_run == -INFINITY) ? 0.f : -m_run * c_log2);
+        ok = mbar_wait(bar(kBarSib + 3 * quad + pb), (nb >> 1) & 1, abort_flag);
+        if (!ok) break;
+        mx = fmaxf(mx, red[(pb * 2 + (half ^ 1)) * kRowsPerTile + row]);
+        {
+          const float m_new = fmaxf(m_run, mx);
+          if (m_new > m_run + rescale_raw) {
+            alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
+            m_run = m_new;
+            compute_p(-m_run * c_log2);
+          }
         }
         float sum8[8];
 #pragma unroll
