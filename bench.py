@@ -473,6 +473,69 @@ def run_sweep(args):
             del kc_alloc, kc
 
 
+def run_cache_ops(args):
+    """Throughput of the cache maintenance next to the decode (mla_write_cache,
+    mla_copy_blocks) on 640-element entries: one decode step's new tokens
+    (b=128), a prefill-sized write (65536 tokens), and copy_blocks_mla over 2048
+    page pairs of 4 layer caches.  GB/s counts bytes read + written; L2 is
+    flushed between iterations.  Timing only, it compares nothing."""
+    from mla_decode_attention_03_gb300 import ops
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    status = ops.new_status(dev)
+
+    def timed(fn):
+        for _ in range(5):
+            flush.fill_(1)
+            fn()
+        evs = []
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            e.record()
+            evs.append((a, e))
+        torch.cuda.synchronize()
+        ops.check_status(status)
+        return float(np.median([a.elapsed_time(e) for a, e in evs]))
+
+    num_blocks = 4096
+    kc_alloc = torch.zeros((num_blocks, 64, 1, 640), dtype=torch.bfloat16, device=dev)
+    kc = kc_alloc[..., :576]
+    for tokens, label in ((128, "write_cache: one decode step, b=128"), (65536, "write_cache: 65536 tokens")):
+        kv_c = torch.randn((tokens, 512), generator=gen, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn((tokens, 64), generator=gen, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(num_blocks * 64, generator=gen, device=dev)[:tokens].to(torch.int64)
+        ms = timed(lambda: ops.write_cache(kv_c, k_pe, slots, kc, status))
+        nbytes = tokens * (576 * 2) * 2 + tokens * 8
+        print(json.dumps({"mode": "cache_ops", "op": label, "ms": round(ms, 5),
+                          "GB/s": round(nbytes / 1e6 / ms, 1), "bytes": nbytes}), flush=True)
+    layers = [torch.zeros((num_blocks, 64, 1, 640), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    perm = torch.randperm(num_blocks, generator=gen, device=dev)
+    mapping = torch.stack([perm[:2048], perm[2048:4096]], dim=1).to(torch.int64)
+    ptrs = torch.tensor([c.data_ptr() for c in layers], dtype=torch.int64, device=dev)
+    mapping = mapping.to(dev)
+    lib = ops.load_library()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def copy_step():
+        # the C ABI call with the layer-pointer array already on the device
+        rc = lib.mla_copy_blocks(ptrs.data_ptr(), len(layers), mapping.data_ptr(), mapping.shape[0],
+                                 num_blocks, 64, 640, status.data_ptr(), stream)
+        if rc != 0:
+            raise RuntimeError(f"mla_copy_blocks failed: {rc}")
+
+    ms = timed(copy_step)
+    nbytes = 2 * 4 * 2048 * 64 * 640 * 2
+    print(json.dumps({"mode": "cache_ops", "op": "copy_blocks: 2048 pairs x 4 layers, 640-element entries",
+                      "ms": round(ms, 5), "GB/s": round(nbytes / 1e6 / ms, 1), "bytes": nbytes}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,9 +547,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None,
                     help="comma-separated mean sequence lengths: print one line per (length, stride)")
+    ap.add_argument("--cache-ops", action="store_true",
+                    help="time the cache write and copy_blocks kernels instead of the decode step")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.cache_ops:
+        run_cache_ops(args)
         return
     world, rank, local = dist_setup()
     try:
