@@ -53,6 +53,13 @@ namespace mla {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kFirstSoftmaxWarp = 8;
+// Registers (setmaxnreg): launched at 128 per thread; the issuing warpgroup
+// (warps 4-7) drops to 48 and the staging/sending warpgroup (warps 0-3) to 120,
+// the two softmax warpgroups take the rest: 128*48 + 128*120 + 256*168 <= 512*128.
+constexpr uint32_t kRegsIssue = 48;
+constexpr uint32_t kRegsStage = 120;
+constexpr uint32_t kRegsSoftmax = 168;
 constexpr int kStages = 4;
 constexpr int kPrefetchPages = 4;  // pages pulled into L2 ahead of their TMA load
 constexpr int kKChunk = kPage * 128;           // 64 tokens x 64 dims bf16 (128B swizzle)
@@ -243,13 +250,13 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 5) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 10 && warp < 14 && rows_valid < kRowsPerTile) {
+  if (warp < 4 && rows_valid < kRowsPerTile) {
     // Rope rows the Q tile does not fill stay zero (their outputs are discarded).
-    const int t = tid - 320;
+    const int t = tid;
     for (int off = rows_valid * 64 + t * 16; off < kQRope; off += 128 * 16)
       *reinterpret_cast<uint4*>(gbase + kOffQR + off) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -259,7 +266,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  // Warpgroups: 0-3 stage Q and send the exchange, 4-7 issue TMA and MMA, 8-15
+  // run the softmax.  Each warpgroup sets its register count as a whole.
+  if (warp >= 4 && warp < 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+  if (warp == 4) {
     // ================================================= TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&q_rope);
@@ -324,10 +335,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 5) {
     // ================================================= PV issuer
-    // Warp 1 issues PV and returns exchange slots to the peer; QK is issued by
-    // warps 14 and 15 (even and odd pages).  Splitting the tcgen05.mma issue
+    // Warp 5 issues PV and returns exchange slots to the peer; QK is issued by
+    // warps 6 and 7 (even and odd pages).  Splitting the tcgen05.mma issue
     // over three sub-partitions keeps any one of them from starving the two
     // softmax warps it hosts.
     if (lane == 0) {
@@ -380,13 +391,13 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       drain_wait(bar(kBarDone), 0);
     }
     __syncwarp();
-  } else if (warp >= 14) {
+  } else {
     // ================================================= QK issuers
-    // Warp 14 takes the even pages (S buffer 0, K stages 0 and 2), warp 15 the
+    // Warp 6 takes the even pages (S buffer 0, K stages 0 and 2), warp 7 the
     // odd ones.  QK(k) needs S buffer k&1 back from the softmax (it has read
     // S(k-2)), the page's K stage and its segment's Q.
     if (lane == 0) {
-      const int parity = warp - 14;
+      const int parity = warp - 6;
       const uint64_t d_klat = smem_desc(base + kOffK, 16, 1024, kSwizzle128B);
       const uint64_t d_krope = smem_desc(base + kOffK + 4 * kKChunk, 16, 512, kSwizzle64B);
       const uint64_t d_qlat = smem_desc(base + kOffQL, 16, 1024, kSwizzle128B);
@@ -454,15 +465,17 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       drain_wait(bar(kBarDone), 0);
     }
     __syncwarp();
-  } else if (warp < 10) {
+  }
+  } else if (warp >= kFirstSoftmaxWarp) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ================================================= softmax + epilogue
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;  // token half [32*half, 32*half+32) of every page
-    const int sw = warp - 2;           // softmax warp index: the exchange slot region it owns
+    const int sw = warp - kFirstSoftmaxWarp;  // softmax warp index: the exchange slot region it owns
+    const int half = sw >> 2;                 // token half [32*half, 32*half+32) of every page
     const int lane_i = static_cast<int>(lane);
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
-    const bool leader = (tid == 64);
+    const bool leader = (sw == 0 && lane == 0);
     float* const red = reinterpret_cast<float*>(gbase + kOffRed);  // [3][2][128]
 
     // row -> (query position, head)
@@ -730,8 +743,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     }
     if (!ok) raise_status(P.status, kStatusTimeout);
   } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsStage));
     // ================================================= Q staging + exchange sending
-    // Warps 10-13 stage each segment's Q -- this CTA's 256 latent dims of each
+    // Warps 0-3 stage each segment's Q -- this CTA's 256 latent dims of each
     // row: [0, 192) into tensor memory as bf16 pairs, [192, 256) into shared
     // memory (128B swizzle, K-major) -- and copy every page's staged partial
     // scores into the peer's receive slot with st.async once the peer has
@@ -747,7 +761,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int h = g * P.heads_per_kv + hh;
     const bool row_live = (row < rows_valid) && (j < P.s_q);
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(P.q);
-    const int st_tid = tid - 320;  // 0..127
+    const int st_tid = tid;  // 0..127
     const uint32_t peer_x = cluster_map(base + kOffX, peer);
     const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
     constexpr int kChunks = kXSlot / 16;  // 1088 16-byte chunks per page
@@ -844,7 +858,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   // ---- teardown: everyone is done with tensor memory and with the peer
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 5) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
