@@ -76,8 +76,7 @@ constexpr int kOffX = kOffK + kStages * kKStage;
 constexpr int kOffStg = kOffX + kXSlots * kXSlot;
 constexpr int kOffQL = kOffStg + kXSlot;  // 1024-aligned (128B swizzle atom)
 constexpr int kOffQR = kOffQL + kQLat;
-constexpr int kOffRed = kOffQR + kQRope;         // sibling-warp exchange: [3][2 halves][128 rows] fp32
-constexpr int kOffBar = kOffRed + 3 * 2 * kRowsPerTile * 4;
+constexpr int kOffBar = kOffQR + kQRope;
 
 // barrier slots
 constexpr int kBarFull = 0;
@@ -93,8 +92,7 @@ constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots
 constexpr int kBarXRead = kBarXEmpty + kXSlots;   // kXSlots: softmax warps have read the slot
 constexpr int kBarStgFull = kBarXRead + kXSlots;  // softmax warps have staged the page
 constexpr int kBarStgFree = kBarStgFull + 1;     // sender warps have read the staging slot
-constexpr int kBarSib = kBarStgFree + 1;  // 4 quadrants x 3 (two page parities + epilogue)
-constexpr int kBarDone = kBarSib + 12;
+constexpr int kBarDone = kBarStgFree + 1;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -246,7 +244,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     }
     mbar_init(bar(kBarStgFull), 8);
     mbar_init(bar(kBarStgFree), 4);
-    for (int s = 0; s < 12; ++s) mbar_init(bar(kBarSib + s), 2);
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
   }
@@ -469,14 +466,18 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   } else if (warp >= kFirstSoftmaxWarp) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ================================================= softmax + epilogue
+    // Warp (quad, half) owns the 16 rows 32*quad + 16*half + [0,16) -- lanes of
+    // its tensor-memory quadrant -- over all 64 tokens of every page.  Lane l
+    // holds row (l & 15) and tokens 32*(l >> 4) + [0,32): a row's two halves sit
+    // in lanes l and l^16, so its max and sum need one shuffle and no other warp.
     const int quad = warp & 3;
     const int sw = warp - kFirstSoftmaxWarp;  // softmax warp index: the exchange slot region it owns
-    const int half = sw >> 2;                 // token half [32*half, 32*half+32) of every page
+    const int half = sw >> 2;                 // which 16 lanes of the quadrant
     const int lane_i = static_cast<int>(lane);
-    const int row = 32 * quad + static_cast<int>(lane);
-    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    const int row = 32 * quad + 16 * half + (lane_i & 15);
+    const int tok0 = 32 * (lane_i >> 4);      // this lane's first token of a page
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad + 16 * half) << 16;
     const bool leader = (sw == 0 && lane == 0);
-    float* const red = reinterpret_cast<float*>(gbase + kOffRed);  // [3][2][128]
 
     // row -> (query position, head)
     const int jj = row / P.heads_per_kv;
@@ -496,7 +497,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     wa.start(meta, P.cache_seqlens, P.max_blocks);
     wb.valid = false;
     float m_run = -INFINITY, l_run = 0.f;
-    int lim_a = 0, lim_b = 0, nseg_epi = 0;
+    int lim_a = 0, lim_b = 0;
     int n = 0;
     bool ok = true;
     float a_prev[32];
@@ -516,7 +517,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         tc_fence_after_sync();
         {
           uint32_t s[32];
-          tmem_ld32(tmem + lane_off + kTmemS + 64u * sb + 32u * half, s);
+          tmem_ld16x2_32(tmem + lane_off + kTmemS + 64u * sb, s);
           tmem_wait_ld(s);
 #pragma unroll
           for (int c = 0; c < 32; ++c) a_cur[c] = __uint_as_float(s[c]);
@@ -525,7 +526,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSFree + sb));
 
-        const int t0 = wa.p * kPage + 32 * half;
+        const int t0 = wa.p * kPage + tok0;
         if (t0 + 32 > lim_a) {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
@@ -595,7 +596,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarXRead + slot));
-        const int t0 = wb.p * kPage + 32 * half;
+        const int t0 = wb.p * kPage + tok0;
         if (t0 + 32 > lim_b) {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
@@ -608,19 +609,21 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         for (int c = 8; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
         float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // The sibling warp holds the other 32 tokens of these rows.  Its max is
-        // posted now and read after P has been computed speculatively with the
-        // running max, which stays in force on almost every page; only when the
-        // page moves the max (and on a segment's first page) is P recomputed.
-        const int pb = nb & 1;
-        red[(pb * 2 + half) * kRowsPerTile + row] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSib + 3 * quad + pb));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the row's other 32 tokens
         float alpha = 1.f;
+        {
+          const float m_new = fmaxf(m_run, mx);
+          if (m_new > m_run + rescale_raw) {
+            alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
+            m_run = m_new;
+          }
+        }
         uint32_t pk[16];
-        uint64_t sum2[4];
-        auto compute_p = [&](float neg_mc) {
+        float rsum;
+        {
+          const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
           const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
+          uint64_t sum2[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
 #pragma unroll
@@ -632,24 +635,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
             sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
             pk[c] = pack_bf16x2(e0, e1);
           }
-        };
-        compute_p((m_run == -INFINITY) ? 0.f : -m_run * c_log2);
-        ok = mbar_wait(bar(kBarSib + 3 * quad + pb), (nb >> 1) & 1, abort_flag);
-        if (!ok) break;
-        mx = fmaxf(mx, red[(pb * 2 + (half ^ 1)) * kRowsPerTile + row]);
-        {
-          const float m_new = fmaxf(m_run, mx);
-          if (m_new > m_run + rescale_raw) {
-            alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
-            m_run = m_new;
-            compute_p(-m_run * c_log2);
-          }
-        }
-        float sum8[8];
+          float sum8[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) f2_split(sum2[u], sum8[2 * u], sum8[2 * u + 1]);
-        const float rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        l_run = l_run * alpha + rsum;
+          for (int u = 0; u < 4; ++u) f2_split(sum2[u], sum8[2 * u], sum8[2 * u + 1]);
+          rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        }
+        l_run = l_run * alpha + rsum;  // this lane's 32 tokens; the row sum adds lane l^16's
         // PV of the previous page has to be complete: it read the P buffer, and O
         // is rescaled below.
         if (nb >= 1) {
@@ -657,18 +648,18 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           if (!ok) break;
           tc_fence_after_sync();
         }
-        tmem_st16(tmem + lane_off + kTmemP + 16u * half, pk);
+        tmem_st16x2(tmem + lane_off + kTmemP, pk);
         const bool rescale_o = !wb.first() && alpha != 1.f;
         if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
             uint32_t o[16];
-            const uint32_t t_o = tmem + lane_off + kTmemO + 128u * half + 16u * c;
-            tmem_ld16(t_o, o);
+            const uint32_t t_o = tmem + lane_off + kTmemO + 32u * c;
+            tmem_ld16x2(t_o, o);
             tmem_wait_ld16(o);
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st16(t_o, o);
+            tmem_st16x2(t_o, o);
           }
         }
         tmem_wait_st();
@@ -678,13 +669,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
 
         // ---- epilogue at the end of a segment
         if (wb.last()) {
-          red[(4 + half) * kRowsPerTile + row] = l_run;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarSib + 3 * quad + 2));
-          ok = mbar_wait(bar(kBarSib + 3 * quad + 2), nseg_epi & 1, abort_flag);
-          if (!ok) break;
-          ++nseg_epi;
-          const float l_tot = red[4 * kRowsPerTile + row] + red[5 * kRowsPerTile + row];
+          const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
           ok = mbar_wait(bar(kBarOFull), nb & 1, abort_flag);
           if (!ok) break;
           tc_fence_after_sync();
@@ -695,11 +680,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + wb.i)) + wb.k;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
+            // columns [64c, 64c+64) of this CTA's half: lane l takes 32 of them
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + kTmemO + 128u * half + 32u * c, o);
+            tmem_ld16x2_32(tmem + lane_off + kTmemO + 64u * c, o);
             tmem_wait_ld(o);
             if (row_live) {
-              const int col = 256 * static_cast<int>(rank) + 128 * half + 32 * c;
+              const int col = 256 * static_cast<int>(rank) + 64 * c + 32 * (lane_i >> 4);
               if (direct) {
                 uint4* dstp = reinterpret_cast<uint4*>(
                     static_cast<__nv_bfloat16*>(P.out) +
@@ -723,7 +709,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
               }
             }
           }
-          if (row_live && rank == 0 && half == 0) {
+          if (row_live && rank == 0 && lane_i < 16) {
             if (direct)
               P.lse[(static_cast<int64_t>(wb.i) * P.h_q + h) * P.s_q + j] = lse;
             else

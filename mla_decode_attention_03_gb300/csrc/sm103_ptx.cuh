@@ -348,7 +348,37 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       MLA_W8(0), MLA_W8(8)
       : "memory");
 }
+
+// Half-quadrant shapes (16x32bx2): a warp addresses 16 lanes -- either half of
+// its 32-lane quadrant -- and two threads share each lane: thread t holds lane
+// (t & 15), columns [S*(t >> 4), S*(t >> 4) + N) from the address, where N is
+// the number of registers and S the half offset.
+__device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t (&r)[16]) {  // N = S = 16
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      MLA_W8(0), MLA_W8(8)
+      : "memory");
+}
 #undef MLA_W8
+#define MLA_R8(b) "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), \
+                  "=r"(r[b + 4]), "=r"(r[b + 5]), "=r"(r[b + 6]), "=r"(r[b + 7])
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[16]) {  // N = S = 16
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;"
+      : MLA_R8(0), MLA_R8(8)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]) {  // N = S = 32
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 32;"
+      : MLA_R8(0), MLA_R8(8), MLA_R8(16), MLA_R8(24)
+      : "r"(taddr));
+}
+#undef MLA_R8
 
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 v;
