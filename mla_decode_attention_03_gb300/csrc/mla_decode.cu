@@ -29,18 +29,23 @@
 //    each), one P buffer (32 columns of packed bf16 that feed PV straight from
 //    tensor memory) and 192 of the CTA's 256 latent Q dims (96 columns); the
 //    other 64 latent Q dims and the rope quarter sit in shared memory.
-//  * Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma and owns
-//    tensor memory, warps 2-9 do the online softmax and the epilogue (warps w
-//    and w+4 share a tensor-memory lane quadrant and take 32 tokens each of the
-//    same 32 rows), warps 10-13 stage each sequence's Q.
+//  * Warp roles per CTA (four warpgroups, registers moved by setmaxnreg):
+//    warps 0-3 stage each sequence's Q and copy the staged partials to the
+//    peer; warp 4 issues TMA; warp 5 issues PV and owns tensor memory; warps
+//    6 and 7 issue QK for even and odd pages; warps 8-15 run the online softmax
+//    and the epilogue, each over 16 full rows (half a tensor-memory lane
+//    quadrant) and all 64 tokens of a page, so a row's max and sum need one
+//    warp shuffle and no other warp.
 //  * The softmax loop is skewed by one page: it reads S(n), quantises and sends
 //    its partial, then finishes page n-1 (whose peer partial arrived meanwhile)
-//    while page n's exchange is in flight.  QK runs two pages ahead of PV; an S
-//    buffer is handed back to the MMA warp as soon as it has been read.
-//  * Exchange slots are returned to the sender by an explicit credit (the
-//    receiver's MMA warp arrives on the sender's barrier once P of that page
-//    exists), so no slot is overwritten before it is read.  All hand-offs are
-//    mbarriers; every wait is bounded.
+//    while page n's exchange is in flight.  QK runs two pages ahead of the
+//    softmax; an S buffer is handed back as soon as it has been read.  The
+//    tensor core executes MMAs in issue order, so QK(n) waits until PV(n-3) has
+//    been issued: PV never queues behind QKs that are not yet needed.
+//  * Exchange slots are returned to the sender by an explicit credit: each
+//    softmax warp that has read its part of a slot arrives (relaxed, remote) on
+//    the sender's barrier, so no slot is overwritten before it is read.  All
+//    hand-offs are mbarriers; every wait is bounded.
 //  * Scores use exp2 with scale*log2(e) folded in; the running max is only
 //    moved (and O rescaled in tensor memory) when it grows by more than 8, so
 //    rescaling is rare.
@@ -88,9 +93,9 @@ constexpr int kBarSFree = kBarSFull + 2;    // 2
 constexpr int kBarPFull = kBarSFree + 2;
 constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
-constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots
-constexpr int kBarXRead = kBarXEmpty + kXSlots;   // kXSlots: softmax warps have read the slot
-constexpr int kBarStgFull = kBarXRead + kXSlots;  // softmax warps have staged the page
+constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: every peer softmax warp has read the slot
+constexpr int kBarPVIssued = kBarXEmpty + kXSlots;  // 2: PV of a page (by parity) has been issued
+constexpr int kBarStgFull = kBarPVIssued + 2;  // softmax warps have staged the page
 constexpr int kBarStgFree = kBarStgFull + 1;     // sender warps have read the staging slot
 constexpr int kBarDone = kBarStgFree + 1;
 constexpr int kNumBars = kBarDone + 1;
@@ -236,11 +241,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarSFree + s), 8);
     }
     mbar_init(bar(kBarPFull), 8);
+    mbar_init(bar(kBarPVIssued), 1);
+    mbar_init(bar(kBarPVIssued + 1), 1);
     mbar_init(bar(kBarOFull), 1);
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(bar(kBarXFull + s), 1);
-      mbar_init(bar(kBarXEmpty + s), 1);
-      mbar_init(bar(kBarXRead + s), 8);
+      mbar_init(bar(kBarXEmpty + s), 8);  // relaxed remote arrivals, one per peer softmax warp
     }
     mbar_init(bar(kBarStgFull), 8);
     mbar_init(bar(kBarStgFree), 4);
@@ -334,54 +340,36 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     __syncwarp();
   } else if (warp == 5) {
     // ================================================= PV issuer
-    // Warp 5 issues PV and returns exchange slots to the peer; QK is issued by
-    // warps 6 and 7 (even and odd pages).  Splitting the tcgen05.mma issue
-    // over three sub-partitions keeps any one of them from starving the two
-    // softmax warps it hosts.
+    // Warp 5 issues PV; QK is issued by warps 6 and 7 (even and odd pages).
+    // Splitting the tcgen05.mma issue over three sub-partitions keeps any one of
+    // them from starving the two softmax warps it hosts.  The tensor core runs
+    // MMAs in issue order, so QK(n) is issued only after PV(n-3): a PV never
+    // queues behind QKs that are not needed yet.
     if (lane == 0) {
       // V = this CTA's 256 latent dims of the page, read MN-major:
       // 64-dim column blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
       const uint64_t d_v = smem_desc(base + kOffK, kKChunk, 1024, kSwizzle128B);
-      const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
       PageWalk wp;
       wp.start(meta, P.cache_seqlens, P.max_blocks);
-      int np = 0, nx = 0;
+      int np = 0;
       bool ok = true;
-      long long t_last = clock64();
       while (wp.valid) {
-        bool issued = true;
-        if (nx <= np && mbar_test(bar(kBarXRead + nx % kXSlots), (nx / kXSlots) & 1)) {
-          // every softmax warp has read the peer's partial of page nx
-          mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nx % kXSlots));
-          ++nx;
-        } else if (mbar_test(bar(kBarPFull), np & 1)) {
-          tc_fence_after_sync();
-          const int st = np % kStages;
-          const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
-          const uint32_t first = wp.first() ? 1u : 0u;
+        ok = mbar_wait(bar(kBarPFull), np & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int st = np % kStages;
+        const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
+        const uint32_t first = wp.first() ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
-                         d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
-                         (first && ks == 0) ? 0u : 1u);
-          umma_commit(bar(kBarEmpty + st));
-          umma_commit(bar(kBarOFull));
-          ++np;
-          wp.advance();
-        } else {
-          issued = false;
-          if (nx <= np)
-            mbar_try_wait_for(bar(kBarXRead + nx % kXSlots), (nx / kXSlots) & 1, 200);
-          else
-            mbar_try_wait_for(bar(kBarPFull), np & 1, 200);
-        }
-        if (issued) {
-          t_last = clock64();
-        } else if (*abort_flag || clock64() - t_last > kWaitTimeoutCycles) {
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
+                       d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
+                       (first && ks == 0) ? 0u : 1u);
+        umma_commit(bar(kBarEmpty + st));
+        umma_commit(bar(kBarOFull));
+        mbar_arrive(bar(kBarPVIssued + (np & 1)));
+        ++np;
+        wp.advance();
       }
       if (!ok) raise_status(P.status, kStatusTimeout);
       umma_commit(bar(kBarDone));
@@ -416,6 +404,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         if ((n & 1) == parity) {
           if (n >= 2) {
             ok = mbar_wait(bar(kBarSFree + parity), ((n >> 1) - 1) & 1, abort_flag);
+            if (!ok) break;
+          }
+          if (n >= 3) {
+            ok = mbar_wait(bar(kBarPVIssued + ((n - 3) & 1)), ((n - 3) >> 1) & 1, abort_flag);
             if (!ok) break;
           }
           const int st = n % kStages;
@@ -478,6 +470,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int tok0 = 32 * (lane_i >> 4);      // this lane's first token of a page
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad + 16 * half) << 16;
     const bool leader = (sw == 0 && lane == 0);
+    const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
 
     // row -> (query position, head)
     const int jj = row / P.heads_per_kv;
@@ -595,20 +588,25 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarXRead + slot));
+        // the slot may be refilled: return it to the peer's sender warps
+        if (lane == 0) mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(slot));
         const int t0 = wb.p * kPage + tok0;
         if (t0 + 32 > lim_b) {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (t0 + c >= lim_b) x[c] = -INFINITY;
         }
-        float mx8[8];
+        float mx4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = x[u];
+        for (int u = 0; u < 4; ++u) mx4[u] = x[u];
 #pragma unroll
-        for (int c = 8; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int c = 4; c < 28; c += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mx4[u] = fmax3(mx4[u], x[c + u], x[c + 4 + u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx4[u] = fmaxf(mx4[u], x[28 + u]);
+        float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the row's other 32 tokens
         float alpha = 1.f;
         {
