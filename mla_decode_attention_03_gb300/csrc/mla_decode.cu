@@ -30,8 +30,8 @@
 //    tensor memory) and 192 of the CTA's 256 latent Q dims (96 columns); the
 //    other 64 latent Q dims and the rope quarter sit in shared memory.
 //  * Warp roles per CTA (four warpgroups, registers moved by setmaxnreg):
-//    warps 0-3 stage each sequence's Q and copy the staged partials to the
-//    peer; warp 4 issues TMA; warp 5 issues PV and owns tensor memory; warps
+//    warps 0-3 stage each sequence's Q and, per page, read the CTA's partial S
+//    out of tensor memory, quantise it and send it to the peer; warp 4 issues TMA; warp 5 issues PV and owns tensor memory; warps
 //    6 and 7 issue QK for even and odd pages; warps 8-15 run the online softmax
 //    and the epilogue, each over 16 full rows (half a tensor-memory lane
 //    quadrant) and all 64 tokens of a page, so a row's max and sum need one
@@ -78,8 +78,7 @@ constexpr int kQLat = kRowsPerTile * 128;      // Q latent dims [192, 256) of th
 
 constexpr int kOffK = 0;
 constexpr int kOffX = kOffK + kStages * kKStage;
-constexpr int kOffStg = kOffX + kXSlots * kXSlot;
-constexpr int kOffQL = kOffStg + kXSlot;  // 1024-aligned (128B swizzle atom)
+constexpr int kOffQL = kOffX + kXSlots * kXSlot;  // 1024-aligned (128B swizzle atom)
 constexpr int kOffQR = kOffQL + kQLat;
 constexpr int kOffBar = kOffQR + kQRope;
 
@@ -95,9 +94,7 @@ constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
 constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: every peer softmax warp has read the slot
 constexpr int kBarPVIssued = kBarXEmpty + kXSlots;  // 2: PV of a page (by parity) has been issued
-constexpr int kBarStgFull = kBarPVIssued + 2;  // softmax warps have staged the page
-constexpr int kBarStgFree = kBarStgFull + 1;     // sender warps have read the staging slot
-constexpr int kBarDone = kBarStgFree + 1;
+constexpr int kBarDone = kBarPVIssued + 2;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -238,7 +235,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     mbar_init(bar(kBarQEmpty), 2);  // both QK issuers
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarSFree + s), 8);
+      mbar_init(bar(kBarSFree + s), 8 + 4);  // softmax warps + sender warps
     }
     mbar_init(bar(kBarPFull), 8);
     mbar_init(bar(kBarPVIssued), 1);
@@ -248,8 +245,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarXFull + s), 1);
       mbar_init(bar(kBarXEmpty + s), 8);  // relaxed remote arrivals, one per peer softmax warp
     }
-    mbar_init(bar(kBarStgFull), 8);
-    mbar_init(bar(kBarStgFree), 4);
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
   }
@@ -497,7 +492,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     while (ok && (wa.valid || wb.valid)) {
       float a_cur[32];
       if (wa.valid) {
-        // ======== page n: own partial out of tensor memory, quantise, send
+        // ======== page n: own partial out of tensor memory (the sender warps
+        // quantise and send the same partial to the peer)
         if (wa.first()) {
           const int L = __ldg(P.cache_seqlens + wa.i);
           lim_a = min(P.causal ? L - P.s_q + j + 1 : L, L);
@@ -518,44 +514,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSFree + sb));
-
-        const int t0 = wa.p * kPage + tok0;
-        if (t0 + 32 > lim_a) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (t0 + c >= lim_a) a_cur[c] = 0.f;
-        }
-        float amax8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) amax8[u] = fabsf(a_cur[u]);
-#pragma unroll
-        for (int c = 8; c < 32; ++c) amax8[c & 7] = fmaxf(amax8[c & 7], fabsf(a_cur[c]));
-        const float amax = fmaxf(fmaxf(fmaxf(amax8[0], amax8[1]), fmaxf(amax8[2], amax8[3])),
-                                 fmaxf(fmaxf(amax8[4], amax8[5]), fmaxf(amax8[6], amax8[7])));
-        const float inv = (amax > 0.f) ? __fdividef(kQuantMax, amax) : 0.f;
-        const uint64_t inv2 = f2(inv, inv), base2 = f2(kQuantBase, kQuantBase);
-        // Stage the encoded partial; the sender warps copy it to the peer while
-        // page n-1 is finished here.
-        if (n >= 1) {
-          ok = mbar_wait(bar(kBarStgFree), (n - 1) & 1, abort_flag);
-          if (!ok) break;
-        }
-        uint8_t* const sp = gbase + kOffStg;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * k + 2 * e;
-            float t0f, t1f;
-            f2_split(f2_fma(f2(a_cur[c], a_cur[c + 1]), inv2, base2), t0f, t1f);
-            wv[e] = __byte_perm(__float_as_uint(t0f), __float_as_uint(t1f), 0x5410);
-          }
-          *reinterpret_cast<uint4*>(sp + x_chunk(sw, lane_i, k)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-        *reinterpret_cast<float*>(sp + x_scale(sw, lane_i)) = amax * (1.0f / kQuantMax);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarStgFull));
       }
 
       if (wb.valid) {
@@ -731,11 +689,14 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     // ================================================= Q staging + exchange sending
     // Warps 0-3 stage each segment's Q -- this CTA's 256 latent dims of each
     // row: [0, 192) into tensor memory as bf16 pairs, [192, 256) into shared
-    // memory (128B swizzle, K-major) -- and copy every page's staged partial
-    // scores into the peer's receive slot with st.async once the peer has
-    // returned that slot: they, not the softmax warps, absorb the SM-to-SM
-    // link's back-pressure.  A segment's Q is staged as soon as the previous
-    // segment's QKs are done, and at the latest before its first page is sent.
+    // memory (128B swizzle, K-major).  Per page, thread `row` reads its row's
+    // 64 partial scores out of tensor memory, quantises each 32-token half and
+    // writes it with st.async into the peer's receive slot, at the place of
+    // the peer softmax thread that owns the row, once the peer has returned
+    // that slot: they, not the softmax warps, do the quantisation and absorb
+    // the SM-to-SM link's back-pressure.  A segment's Q is staged as soon as
+    // the previous segment's QKs are done, and at the latest before its first
+    // page is sent.
     const int quad = warp & 3;
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
@@ -745,11 +706,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int h = g * P.heads_per_kv + hh;
     const bool row_live = (row < rows_valid) && (j < P.s_q);
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(P.q);
-    const int st_tid = tid;  // 0..127
     const uint32_t peer_x = cluster_map(base + kOffX, peer);
     const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
-    constexpr int kChunks = kXSlot / 16;  // 1088 16-byte chunks per page
-    constexpr int kPerThread = (kChunks + 127) / 128;
+    int lim = 0;  // visible tokens of this row in the current sequence
 
     auto load32 = [&](const uint8_t* src, uint32_t (&r)[32]) {
       if (row_live) {
@@ -808,18 +767,52 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         ok = stage_q();
         if (!ok) break;
       }
-      // ---- send page n
-      ok = mbar_wait(bar(kBarStgFull), n & 1, abort_flag);
-      if (!ok) break;
-      uint4 v[kPerThread];
-      const uint8_t* sp = gbase + kOffStg;
-#pragma unroll
-      for (int k = 0; k < kPerThread; ++k) {
-        const int c = st_tid + 128 * k;
-        if (c < kChunks) v[k] = *reinterpret_cast<const uint4*>(sp + 16 * c);
+      // ---- page n: this CTA's partial S of row `row`, quantised per 32 tokens
+      if (w.first()) {
+        const int L = __ldg(P.cache_seqlens + w.i);
+        lim = min(P.causal ? L - P.s_q + j + 1 : L, L);
       }
+      const int sb = n & 1;
+      ok = mbar_wait(bar(kBarSFull + sb), (n >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tmem + lane_off + kTmemS + 64u * sb, s0);
+      tmem_ld32(tmem + lane_off + kTmemS + 64u * sb + 32u, s1);
+      tmem_wait_ld2(s0, s1);
+      tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarStgFree));
+      if (lane == 0) mbar_arrive(bar(kBarSFree + sb));
+      uint32_t enc[2][16];
+      float scl[2];
+#pragma unroll
+      for (int th = 0; th < 2; ++th) {
+        float a[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) a[c] = __uint_as_float(th ? s1[c] : s0[c]);
+        const int t0 = w.p * kPage + 32 * th;
+        if (t0 + 32 > lim) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (t0 + c >= lim) a[c] = 0.f;
+        }
+        float amax8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) amax8[u] = fabsf(a[u]);
+#pragma unroll
+        for (int c = 8; c < 32; ++c) amax8[c & 7] = fmaxf(amax8[c & 7], fabsf(a[c]));
+        const float amax = fmaxf(fmaxf(fmaxf(amax8[0], amax8[1]), fmaxf(amax8[2], amax8[3])),
+                                 fmaxf(fmaxf(amax8[4], amax8[5]), fmaxf(amax8[6], amax8[7])));
+        const float inv = (amax > 0.f) ? __fdividef(kQuantMax, amax) : 0.f;
+        const uint64_t inv2 = f2(inv, inv), base2 = f2(kQuantBase, kQuantBase);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float t0f, t1f;
+          f2_split(f2_fma(f2(a[2 * e], a[2 * e + 1]), inv2, base2), t0f, t1f);
+          enc[th][e] = __byte_perm(__float_as_uint(t0f), __float_as_uint(t1f), 0x5410);
+        }
+        scl[th] = amax * (1.0f / kQuantMax);
+      }
       const int slot = n % kXSlots;
       if (n >= kXSlots) {
         // the peer has read page n - 2 out of the slot page n goes to
@@ -828,10 +821,17 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       }
       const uint32_t dst = peer_x + static_cast<uint32_t>(slot * kXSlot);
       const uint32_t xb = peer_xfull + 8u * static_cast<uint32_t>(slot);
+      // the peer's softmax warp (quad, lane >> 4) owns this row; its lanes
+      // (lane & 15) and (lane & 15) + 16 take tokens [0, 32) and [32, 64)
+      const int rsw = quad + 4 * static_cast<int>(lane >> 4);
 #pragma unroll
-      for (int k = 0; k < kPerThread; ++k) {
-        const int c = st_tid + 128 * k;
-        if (c < kChunks) st_async_v4(dst + 16u * static_cast<uint32_t>(c), v[k].x, v[k].y, v[k].z, v[k].w, xb);
+      for (int th = 0; th < 2; ++th) {
+        const int rl = static_cast<int>(lane & 15) + 16 * th;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_async_v4(dst + x_chunk(rsw, rl, k), enc[th][4 * k], enc[th][4 * k + 1], enc[th][4 * k + 2],
+                      enc[th][4 * k + 3], xb);
+        st_async_b32(dst + x_scale(rsw, rl), __float_as_uint(scl[th]), xb);
       }
       ++n;
       w.advance();
