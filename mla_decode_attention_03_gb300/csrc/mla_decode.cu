@@ -42,9 +42,11 @@
 //    softmax; an S buffer is handed back as soon as it has been read.  The
 //    tensor core executes MMAs in issue order, so QK(n) waits until PV(n-3) has
 //    been issued: PV never queues behind QKs that are not yet needed.
-//  * Exchange slots are returned to the sender by an explicit credit: each
-//    softmax warp that has read its part of a slot arrives (relaxed, remote) on
-//    the sender's barrier, so no slot is overwritten before it is read.  All
+//  * Exchange slots are returned to the sender by an explicit credit: once
+//    all softmax warps have read a slot (a local barrier), sender warp 0
+//    forwards a relaxed remote arrive to the peer's sender barrier, so no slot
+//    is overwritten before it is read.  (A release-ordered remote arrive from
+//    every softmax warp cost 70 us per decode; an unordered one raced.)  All
 //    hand-offs are mbarriers; every wait is bounded.
 //  * Scores use exp2 with scale*log2(e) folded in; the running max is only
 //    moved (and O rescaled in tensor memory) when it grows by more than 8, so
@@ -92,8 +94,9 @@ constexpr int kBarSFree = kBarSFull + 2;    // 2
 constexpr int kBarPFull = kBarSFree + 2;
 constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
-constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: every peer softmax warp has read the slot
-constexpr int kBarPVIssued = kBarXEmpty + kXSlots;  // 2: PV of a page (by parity) has been issued
+constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: the peer has read the slot (relayed credit)
+constexpr int kBarXRead = kBarXEmpty + kXSlots;   // kXSlots: this CTA's softmax warps have read the slot
+constexpr int kBarPVIssued = kBarXRead + kXSlots;  // 2: PV of a page (by parity) has been issued
 constexpr int kBarDone = kBarPVIssued + 2;
 constexpr int kNumBars = kBarDone + 1;
 
@@ -243,7 +246,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     mbar_init(bar(kBarOFull), 1);
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(bar(kBarXFull + s), 1);
-      mbar_init(bar(kBarXEmpty + s), 8);  // relaxed remote arrivals, one per peer softmax warp
+      mbar_init(bar(kBarXEmpty + s), 1);
+      mbar_init(bar(kBarXRead + s), 8);
     }
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
@@ -293,6 +297,25 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         wpf.advance();
       };
       for (int a = 0; a < kPrefetchPages; ++a) prefetch_next();
+      // The Q rows of every later segment of this part go to L2 now: a
+      // segment's Q is staged only once the previous segment's QKs are done,
+      // and read from HBM that staging stalled the pipeline for microseconds.
+      {
+        PageWalk ws = w;
+        if (ws.valid) ws.next_segment();
+        const uint8_t* const qb = static_cast<const uint8_t*>(P.q);
+        const uint32_t row_bytes = static_cast<uint32_t>(P.heads_per_kv) * kDimQK * 2u;
+        for (; ws.valid; ws.next_segment()) {
+          for (int jj = 0; jj < P.q_per_tile; ++jj) {
+            const int jq = tile * P.q_per_tile + jj;
+            if (jq >= P.s_q) break;
+            const uint8_t* src = qb + ((static_cast<int64_t>(ws.i) * P.s_q + jq) * P.h_q +
+                                       static_cast<int64_t>(g) * P.heads_per_kv) * (kDimQK * 2);
+            for (uint32_t off = 0; off < row_bytes; off += 16384u)
+              bulk_prefetch_l2(src + off, min(16384u, row_bytes - off));
+          }
+        }
+      }
       int n = 0, seg = 0;
       bool ok = true;
       while (w.valid && ok) {
@@ -465,7 +488,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int tok0 = 32 * (lane_i >> 4);      // this lane's first token of a page
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad + 16 * half) << 16;
     const bool leader = (sw == 0 && lane == 0);
-    const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
 
     // row -> (query position, head)
     const int jj = row / P.heads_per_kv;
@@ -545,9 +567,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
             }
           }
         }
+        // the slot has been read (sender warp 0 returns it to the peer)
         __syncwarp();
-        // the slot may be refilled: return it to the peer's sender warps
-        if (lane == 0) mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(slot));
+        if (lane == 0) mbar_arrive(bar(kBarXRead + slot));
         const int t0 = wb.p * kPage + tok0;
         if (t0 + 32 > lim_b) {
 #pragma unroll
@@ -756,17 +778,41 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       wq.next_segment();
       return true;
     };
-    int n = 0, seg = 0;
-    while (ok && w.valid) {
-      if (w.first() && n > 0) ++seg;
-      // this page's segment needs its Q before its page can be staged
-      while (ok && wq.valid && qseg <= seg) ok = stage_q();
-      if (!ok) break;
-      // the next segment's Q, as soon as its slot is free
-      if (wq.valid && qseg == seg + 1 && mbar_test(bar(kBarQEmpty), (qseg & 1) ^ 1)) {
-        ok = stage_q();
-        if (!ok) break;
+    // The warps poll: a segment's Q is staged the moment the previous
+    // segment's QKs are done (its first page's QK waits for it), otherwise the
+    // next page is sent once its S is ready.  Staging never waits behind a
+    // send, whose slot credit depends on the peer's progress.  Each decision is
+    // lane 0's, broadcast, so the warp stays converged.
+    // Warp 0 also returns exchange slots to the peer: slot credit for page nr
+    // once every softmax warp has read the peer's partial of page nr.
+    const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
+    int n = 0, nr = 0;
+    long long t_idle = clock64();
+    while (ok && (w.valid || wq.valid || (warp == 0 && nr < n))) {
+      if (warp == 0 && nr < n + (w.valid ? 1 : 0) &&
+          __shfl_sync(0xffffffffu, mbar_test(bar(kBarXRead + nr % kXSlots), (nr / kXSlots) & 1) ? 1 : 0, 0)) {
+        if (lane == 0) mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nr % kXSlots));
+        ++nr;
+        t_idle = clock64();
+        continue;
       }
+      if (__shfl_sync(0xffffffffu, (wq.valid && mbar_test(bar(kBarQEmpty), (qseg & 1) ^ 1)) ? 1 : 0, 0)) {
+        ok = stage_q();
+        t_idle = clock64();
+        continue;
+      }
+      if (!w.valid || !__shfl_sync(0xffffffffu, mbar_test(bar(kBarSFull + (n & 1)), (n >> 1) & 1) ? 1 : 0, 0)) {
+        if (w.valid) mbar_try_wait_for(bar(kBarSFull + (n & 1)), (n >> 1) & 1, 200);
+        else if (wq.valid) mbar_try_wait_for(bar(kBarQEmpty), (qseg & 1) ^ 1, 200);
+        else mbar_try_wait_for(bar(kBarXRead + nr % kXSlots), (nr / kXSlots) & 1, 200);
+        int give_up = (*abort_flag || clock64() - t_idle > kWaitTimeoutCycles) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, give_up, 0)) {
+          *abort_flag = 1;
+          ok = false;
+        }
+        continue;
+      }
+      t_idle = clock64();
       // ---- page n: this CTA's partial S of row `row`, quantised per 32 tokens
       if (w.first()) {
         const int L = __ldg(P.cache_seqlens + w.i);
@@ -815,8 +861,24 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       }
       const int slot = n % kXSlots;
       if (n >= kXSlots) {
-        // the peer has read page n - 2 out of the slot page n goes to
-        ok = mbar_wait<true>(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, abort_flag);
+        // The peer has read page n - 2 out of the slot page n goes to.  Warp 0
+        // keeps returning this CTA's slots while it waits: the peer's senders
+        // may be waiting for them in the same way.
+        const long long t_wait = clock64();
+        while (true) {
+          const bool got = mbar_try_wait_cluster_for(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, 100);
+          if (__all_sync(0xffffffffu, got)) break;
+          if (warp == 0 && nr <= n &&
+              __shfl_sync(0xffffffffu, mbar_test(bar(kBarXRead + nr % kXSlots), (nr / kXSlots) & 1) ? 1 : 0, 0)) {
+            if (lane == 0) mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nr % kXSlots));
+            ++nr;
+          }
+          if (__shfl_sync(0xffffffffu, (*abort_flag || clock64() - t_wait > kWaitTimeoutCycles) ? 1 : 0, 0)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+        }
         if (!ok) break;
       }
       const uint32_t dst = peer_x + static_cast<uint32_t>(slot * kXSlot);

@@ -194,6 +194,13 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int c0, int 
                : "memory");
 }
 
+// Pulls `bytes` (a multiple of 16) of global memory at a 16-byte aligned
+// address into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
