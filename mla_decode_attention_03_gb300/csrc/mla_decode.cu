@@ -42,11 +42,12 @@
 //    softmax; an S buffer is handed back as soon as it has been read.  The
 //    tensor core executes MMAs in issue order, so QK(n) waits until PV(n-3) has
 //    been issued: PV never queues behind QKs that are not yet needed.
-//  * Exchange slots are returned to the sender by an explicit credit: once
-//    all softmax warps have read a slot (a local barrier), sender warp 0
-//    forwards a relaxed remote arrive to the peer's sender barrier, so no slot
-//    is overwritten before it is read.  (A release-ordered remote arrive from
-//    every softmax warp cost 70 us per decode; an unordered one raced.)  All
+//  * Exchange slots are returned to the sender by an explicit credit: each
+//    softmax warp that has read its part of a slot fences (CTA scope) and
+//    counts; the warp that completes the count of 8 sends one relaxed remote
+//    arrive to the peer's sender barrier, so no slot is overwritten before it
+//    is read.  (A release-ordered remote arrive from every warp cost 70 us per
+//    decode; an unordered relaxed one from every warp raced.)  All
 //    hand-offs are mbarriers; every wait is bounded.
 //  * Scores use exp2 with scale*log2(e) folded in; the running max is only
 //    moved (and O rescaled in tensor memory) when it grows by more than 8, so
@@ -94,14 +95,13 @@ constexpr int kBarSFree = kBarSFull + 2;    // 2
 constexpr int kBarPFull = kBarSFree + 2;
 constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
-constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: the peer has read the slot (relayed credit)
-constexpr int kBarXRead = kBarXEmpty + kXSlots;   // kXSlots: this CTA's softmax warps have read the slot
-constexpr int kBarPVIssued = kBarXRead + kXSlots;  // 2: PV of a page (by parity) has been issued
+constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: the peer has read the slot
+constexpr int kBarPVIssued = kBarXEmpty + kXSlots;  // 2: PV of a page (by parity) has been issued
 constexpr int kBarDone = kBarPVIssued + 2;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemUsed = kOffMisc + 16 + 8;  // tmem slot, abort flag, pad, two slot-read counters
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kOffQL % 1024 == 0, "Q latent tile must sit on a 128B-swizzle atom");
 static_assert(kOffQR % 512 == 0, "Q rope tile must sit on a 64B-swizzle atom");
@@ -215,6 +215,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   auto bar = [&](int idx) -> uint32_t { return base + kOffBar + 8u * idx; };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + kOffMisc + 4);
+  uint32_t* const xread_cnt = reinterpret_cast<uint32_t*>(gbase + kOffMisc + 16);  // [kXSlots]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -230,6 +231,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   // ---- setup
   if (tid == 0) {
     *abort_flag = 0;
+    for (int s = 0; s < kXSlots; ++s) xread_cnt[s] = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
@@ -247,7 +249,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(bar(kBarXFull + s), 1);
       mbar_init(bar(kBarXEmpty + s), 1);
-      mbar_init(bar(kBarXRead + s), 8);
     }
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
     fence_mbar_init();
@@ -488,6 +489,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int tok0 = 32 * (lane_i >> 4);      // this lane's first token of a page
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad + 16 * half) << 16;
     const bool leader = (sw == 0 && lane == 0);
+    const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
 
     // row -> (query position, head)
     const int jj = row / P.heads_per_kv;
@@ -567,9 +569,19 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
             }
           }
         }
-        // the slot has been read (sender warp 0 returns it to the peer)
+        // The slot has been read: the last of the 8 softmax warps to finish
+        // returns it to the peer's senders.  Each warp's fence orders its lanes'
+        // loads (after the warp barrier) before its count; the last warp's fence
+        // orders all of them before its remote arrive.
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarXRead + slot));
+        if (lane == 0) {
+          __threadfence_block();
+          if (atomicAdd(xread_cnt + slot, 1u) == 7u) {
+            xread_cnt[slot] = 0u;
+            __threadfence_block();
+            mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(slot));
+          }
+        }
         const int t0 = wb.p * kPage + tok0;
         if (t0 + 32 > lim_b) {
 #pragma unroll
@@ -783,19 +795,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     // next page is sent once its S is ready.  Staging never waits behind a
     // send, whose slot credit depends on the peer's progress.  Each decision is
     // lane 0's, broadcast, so the warp stays converged.
-    // Warp 0 also returns exchange slots to the peer: slot credit for page nr
-    // once every softmax warp has read the peer's partial of page nr.
-    const uint32_t peer_xempty = cluster_map(bar(kBarXEmpty), peer);
-    int n = 0, nr = 0;
+    int n = 0;
     long long t_idle = clock64();
-    while (ok && (w.valid || wq.valid || (warp == 0 && nr < n))) {
-      if (warp == 0 && nr < n + (w.valid ? 1 : 0) &&
-          __shfl_sync(0xffffffffu, mbar_test(bar(kBarXRead + nr % kXSlots), (nr / kXSlots) & 1) ? 1 : 0, 0)) {
-        if (lane == 0) mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nr % kXSlots));
-        ++nr;
-        t_idle = clock64();
-        continue;
-      }
+    while (ok && (w.valid || wq.valid)) {
       if (__shfl_sync(0xffffffffu, (wq.valid && mbar_test(bar(kBarQEmpty), (qseg & 1) ^ 1)) ? 1 : 0, 0)) {
         ok = stage_q();
         t_idle = clock64();
@@ -803,8 +805,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       }
       if (!w.valid || !__shfl_sync(0xffffffffu, mbar_test(bar(kBarSFull + (n & 1)), (n >> 1) & 1) ? 1 : 0, 0)) {
         if (w.valid) mbar_try_wait_for(bar(kBarSFull + (n & 1)), (n >> 1) & 1, 200);
-        else if (wq.valid) mbar_try_wait_for(bar(kBarQEmpty), (qseg & 1) ^ 1, 200);
-        else mbar_try_wait_for(bar(kBarXRead + nr % kXSlots), (nr / kXSlots) & 1, 200);
+        else mbar_try_wait_for(bar(kBarQEmpty), (qseg & 1) ^ 1, 200);
         int give_up = (*abort_flag || clock64() - t_idle > kWaitTimeoutCycles) ? 1 : 0;
         if (__shfl_sync(0xffffffffu, give_up, 0)) {
           *abort_flag = 1;
@@ -861,24 +862,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       }
       const int slot = n % kXSlots;
       if (n >= kXSlots) {
-        // The peer has read page n - 2 out of the slot page n goes to.  Warp 0
-        // keeps returning this CTA's slots while it waits: the peer's senders
-        // may be waiting for them in the same way.
-        const long long t_wait = clock64();
-        while (true) {
-          const bool got = mbar_try_wait_cluster_for(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, 100);
-          if (__all_sync(0xffffffffu, got)) break;
-          if (warp == 0 && nr <= n &&
-              __shfl_sync(0xffffffffu, mbar_test(bar(kBarXRead + nr % kXSlots), (nr / kXSlots) & 1) ? 1 : 0, 0)) {
-            if (lane == 0) mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(nr % kXSlots));
-            ++nr;
-          }
-          if (__shfl_sync(0xffffffffu, (*abort_flag || clock64() - t_wait > kWaitTimeoutCycles) ? 1 : 0, 0)) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-        }
+        // the peer has read page n - 2 out of the slot page n goes to
+        ok = mbar_wait<true>(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, abort_flag);
         if (!ok) break;
       }
       const uint32_t dst = peer_x + static_cast<uint32_t>(slot * kXSlot);
