@@ -101,7 +101,7 @@ constexpr int kBarDone = kBarPVIssued + 2;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffMisc + 16 + 8;  // tmem slot, abort flag, pad, two slot-read counters
+constexpr int kSmemUsed = kOffMisc + 16 + 4 * kXSlots;  // tmem slot, abort flag, pad, slot-read counters
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kOffQL % 1024 == 0, "Q latent tile must sit on a 128B-swizzle atom");
 static_assert(kOffQR % 512 == 0, "Q rope tile must sit on a 64B-swizzle atom");
