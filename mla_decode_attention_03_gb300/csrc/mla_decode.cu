@@ -69,7 +69,6 @@ constexpr uint32_t kRegsIssue = 48;
 constexpr uint32_t kRegsStage = 120;
 constexpr uint32_t kRegsSoftmax = 168;
 constexpr int kStages = 4;
-constexpr int kPrefetchPages = 4;  // pages pulled into L2 ahead of their TMA load
 constexpr int kKChunk = kPage * 128;           // 64 tokens x 64 dims bf16 (128B swizzle)
 constexpr int kKRope = kPage * 64;             // 64 tokens x 32 dims bf16 (64B swizzle)
 constexpr int kKStage = 4 * kKChunk + kKRope;  // 36864 bytes: this CTA's 288 dims of a page
@@ -282,22 +281,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       const uint64_t evict_first = l2_policy_evict_first();
       const int dim_lat = 256 * static_cast<int>(rank);
       const int dim_rope = 512 + 32 * static_cast<int>(rank);
-      PageWalk w, wpf;
+      PageWalk w;
       w.start(meta, P.cache_seqlens, P.max_blocks);
-      wpf = w;
-      // L2 prefetch runs kPrefetchPages ahead of the loads, which then hit L2:
-      // that shortens the load latency the stage ring has to cover.
-      auto prefetch_next = [&]() {
-        if (!wpf.valid) return;
-        const int ph = __ldg(P.block_table + static_cast<int64_t>(wpf.i) * P.max_blocks + wpf.p);
-        if (ph >= 0 && ph < P.num_blocks) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&k_lat, dim_lat + 64 * c, g, ph * kPage);
-          tma_prefetch_l2_3d(&k_rope, dim_rope, g, ph * kPage);
-        }
-        wpf.advance();
-      };
-      for (int a = 0; a < kPrefetchPages; ++a) prefetch_next();
+      // (Prefetching pages into L2 ahead of their TMA loads was measured and
+      // dropped: 2, 4 and 8 pages ahead all ran slower than none.)
       // The Q rows of every later segment of this part go to L2 now: a
       // segment's Q is staged only once the previous segment's QKs are done,
       // and read from HBM that staging stalled the pipeline for microseconds.
@@ -320,7 +307,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       int n = 0, seg = 0;
       bool ok = true;
       while (w.valid && ok) {
-        prefetch_next();
         if (w.first()) {
           ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
           if (!ok) break;

@@ -186,13 +186,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
-// Pulls a tile into L2 only (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 
 // Pulls `bytes` (a multiple of 16) of global memory at a 16-byte aligned
 // address into L2 (no shared memory, no barrier).
