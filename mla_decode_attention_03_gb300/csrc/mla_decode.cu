@@ -267,6 +267,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   cluster_sync();  // barriers of both CTAs are initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel (the scheduler); nothing it
+  // wrote is read before this point.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // Warpgroups: 0-3 stage Q and send the exchange, 4-7 issue TMA and MMA, 8-15
   // run the softmax.  Each warpgroup sets its register count as a whole.
@@ -897,9 +901,19 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_rope, cons
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(2 * num_parts, row_tiles, p.h_kv);
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_rope, k_lat, k_rope, p);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the CTAs start (tensor memory,
+  // barriers, cluster sync) while the scheduler kernel before them finishes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_parts, row_tiles, p.h_kv);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, q_rope, k_lat, k_rope, p);
 }
 
 cudaError_t decode_max_active_clusters(int* clusters) {

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
   extern __shared__ int64_t C[];  // [b + 1]: cost prefix
   __shared__ int64_t buf64[kMetaThreads / 32];
   __shared__ int32_t buf32[kMetaThreads / 32];
+  grid_launch_dependents();  // the decode kernel's CTAs may start their set-up
   const int tid = threadIdx.x;
   const int chunk = (b + kMetaThreads - 1) / kMetaThreads;
   const int lo = min(b, tid * chunk), hi = min(b, lo + chunk);
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // written directly by the decode kernel; sequences with none (length 0) get
 // out = 0 and lse = -inf.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams P) {
+  grid_dependency_wait();  // the decode kernel's partials are complete and visible
   const int i = blockIdx.x;
   const int rows = P.s_q * P.h_q;
   const int row = blockIdx.y * 4 + (threadIdx.x >> 5);
@@ -249,9 +252,16 @@ cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, 
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   const int rows = p.s_q * p.h_q;
-  dim3 grid(p.b, (rows + 3) / 4);
-  mla_combine_kernel<<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.b, (rows + 3) / 4, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
 }
 
 }  // namespace mla

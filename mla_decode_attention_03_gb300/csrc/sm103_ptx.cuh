@@ -147,6 +147,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the
+// previous kernel in the stream is still running; it must wait here before it
+// reads anything that kernel wrote.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream (if launched that way) start launching.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ proxy fences
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor-core operands).
