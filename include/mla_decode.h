@@ -81,7 +81,8 @@ size_t mla_metadata_ints(int num_parts);
 
 /*
  * Bytes of scratch the decode call needs for split partial results:
- * (b + num_parts) x s_q x h_q x (512 + 1) fp32 values, plus alignment.
+ * (b + num_parts) x s_q x h_q x 512 bf16 partial outputs, then
+ * (b + num_parts) x s_q x h_q fp32 partial lse, each block 256-byte aligned.
  */
 size_t mla_workspace_bytes(int b, int s_q, int h_q, int num_parts);
 
@@ -144,7 +145,7 @@ mla_status_t mla_decode_with_kvcache(const void *q, int b, int s_q, int h_q, int
  * schedule them separately.  mla_decode_splitkv takes the same arguments and
  * runs only the decode kernel: sequences cut into one piece get their out and
  * lse written directly; the pieces of the others go to `workspace` as
- * normalised fp32 partial outputs and natural-log partial lse.
+ * normalised bf16 partial outputs and fp32 natural-log partial lse.
  * mla_combine_splits then merges those pieces by their log-sum-exps (the
  * Flash-Decoding merge) into out and lse, and writes out = 0, lse = -inf for
  * sequences of length 0.  It must run after mla_decode_splitkv on the same

@@ -48,7 +48,7 @@ Shape tile_shape(int s_q, int h_q, int h_kv) {
 
 size_t workspace_o_bytes(int b, int s_q, int h_q, int num_parts) {
   const size_t slots = static_cast<size_t>(b) + static_cast<size_t>(num_parts);
-  const size_t bytes = slots * static_cast<size_t>(s_q) * h_q * kDimV * sizeof(float);
+  const size_t bytes = slots * static_cast<size_t>(s_q) * h_q * kDimV * 2;  // bf16 partials
   return (bytes + 255) & ~static_cast<size_t>(255);
 }
 
@@ -185,7 +185,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
     if (r != MLA_OK) return r;
   }
 
-  float* ws_o = static_cast<float*>(workspace);
+  void* ws_o = workspace;
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            workspace_o_bytes(b, s_q, h_q, num_parts));
   mla::DecodeParams p;
@@ -288,7 +288,7 @@ mla_status_t mla_combine_splits(const int32_t* num_splits, int b, int s_q, int h
     return MLA_ERR_ALIGNMENT;
   mla::CombineParams c;
   c.num_splits = num_splits;
-  c.ws_o = static_cast<const float*>(workspace);
+  c.ws_o = workspace;
   c.ws_lse = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
                                             workspace_o_bytes(b, s_q, h_q, num_parts));
   c.out = out;

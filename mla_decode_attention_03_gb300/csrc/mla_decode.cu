@@ -666,26 +666,21 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
             tmem_wait_ld(o);
             if (row_live) {
               const int col = 256 * static_cast<int>(rank) + 64 * c + 32 * (lane_i >> 4);
-              if (direct) {
-                uint4* dstp = reinterpret_cast<uint4*>(
-                    static_cast<__nv_bfloat16*>(P.out) +
-                    ((static_cast<int64_t>(wb.i) * rows_total + row_in_seq) * kDimV + col));
+              // single-split sequences go straight to out, the pieces of the
+              // others to the workspace (bf16, normalised by their own sums)
+              __nv_bfloat16* const dst_row =
+                  direct ? static_cast<__nv_bfloat16*>(P.out) +
+                               ((static_cast<int64_t>(wb.i) * rows_total + row_in_seq) * kDimV + col)
+                         : static_cast<__nv_bfloat16*>(P.ws_o) + ((oslot * rows_total + row_in_seq) * kDimV + col);
+              uint4* dstp = reinterpret_cast<uint4*>(dst_row);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  uint4 v;
-                  v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-                  v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-                  v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-                  v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-                  dstp[q] = v;
-                }
-              } else {
-                float4* dstp = reinterpret_cast<float4*>(
-                    P.ws_o + ((oslot * rows_total + row_in_seq) * kDimV + col));
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  dstp[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                        __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+              for (int q = 0; q < 4; ++q) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+                dstp[q] = v;
               }
             }
           }
