@@ -150,6 +150,12 @@ mla_status_t mla_decode_with_kvcache(const void *q, int b, int s_q, int h_q, int
  * Flash-Decoding merge) into out and lse, and writes out = 0, lse = -inf for
  * sequences of length 0.  It must run after mla_decode_splitkv on the same
  * workspace, b, s_q, h_q and num_parts; ordering on one stream suffices.
+ *
+ * Both kernels are launched with programmatic dependent launch: they may
+ * start their set-up (shared and tensor memory only) while the kernel before
+ * them on the stream is still running, and wait for that kernel to complete
+ * before they read or write any global memory, so stream order keeps its
+ * usual meaning for the caller.
  */
 mla_status_t mla_decode_splitkv(const void *q, int b, int s_q, int h_q, int d,
                                 const void *kcache, int64_t num_blocks, int block_size,
