@@ -31,14 +31,15 @@
 //    other 64 latent Q dims and the rope quarter sit in shared memory.
 //  * Warp roles per CTA (four warpgroups, registers moved by setmaxnreg):
 //    warps 0-3 stage each sequence's Q and, per page, read the CTA's partial S
-//    out of tensor memory, quantise it and send it to the peer; warp 4 issues TMA; warp 5 issues PV and owns tensor memory; warps
-//    6 and 7 issue QK for even and odd pages; warps 8-15 run the online softmax
+//    out of tensor memory, quantise it and send it to the peer; warp 4 issues
+//    TMA; warp 5 issues PV and owns tensor memory; warps 6 and 7 issue QK for
+//    even and odd pages; warps 8-15 run the online softmax
 //    and the epilogue, each over 16 full rows (half a tensor-memory lane
 //    quadrant) and all 64 tokens of a page, so a row's max and sum need one
 //    warp shuffle and no other warp.
-//  * The softmax loop is skewed by one page: it reads S(n), quantises and sends
-//    its partial, then finishes page n-1 (whose peer partial arrived meanwhile)
-//    while page n's exchange is in flight.  QK runs two pages ahead of the
+//  * The softmax loop is skewed by one page: it reads its partial S(n) (which
+//    the sender warps quantise and send meanwhile), then finishes page n-1,
+//    whose peer partial arrived while it worked on page n.  QK runs two pages ahead of the
 //    softmax; an S buffer is handed back as soon as it has been read.  The
 //    tensor core executes MMAs in issue order, so QK(n) waits until PV(n-3) has
 //    been issued: PV never queues behind QKs that are not yet needed.
@@ -47,7 +48,7 @@
 //    counts; the warp that completes the count of 8 sends one relaxed remote
 //    arrive to the peer's sender barrier, so no slot is overwritten before it
 //    is read.  (A release-ordered remote arrive from every warp cost 70 us per
-//    decode; an unordered relaxed one from every warp raced.)  All
+//    decode; an unordered relaxed one from every warp raced.)  All other
 //    hand-offs are mbarriers; every wait is bounded.
 //  * Scores use exp2 with scale*log2(e) folded in; the running max is only
 //    moved (and O rescaled in tensor memory) when it grows by more than 8, so
