@@ -45,7 +45,7 @@ BREAKDOWN_EVERY = 8  # every 8th timed step also times each kernel on its own
 # taken from one ncu capture, keyed by a digest of the kernel's sources (comments
 # and whitespace ignored) and by the workload (name, entry stride).  A kernel
 # whose code changed since the capture reports null traffic.
-KERNEL_SOURCES = ("mla_decode.cu", "sm103_ptx.cuh")
+KERNEL_SOURCES = ("mla_decode.cu", "sm103_ptx.cuh", "mla_sched.cu", "mla_internal.h")
 MEASURED_TRAFFIC = {
     ("bcf06acbe85794d0", "bench", 576): 627208704,
 }

@@ -12,7 +12,7 @@ constexpr int kDimV = 512;      // value = leading 512 latent dims
 constexpr int kPage = 64;       // tokens per cache page
 constexpr int kRowsPerTile = 128;
 constexpr int kMetaInts = 8;    // ints per scheduler part
-constexpr int kSegmentCost = 2; // fixed scheduler cost of one (sequence, part) segment, in pages
+constexpr int kSegmentCost = 6; // fixed scheduler cost of one (sequence, part) segment, in pages (measured: 2, 4, 6, 8, 12 -> 6 best)
 constexpr int kMinPartPages = 8;
 constexpr int kMaxMetadataBatch = 16384;  // sequences the scheduler stages in shared memory
 

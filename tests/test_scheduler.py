@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-SEGMENT_COST, MIN_PART_PAGES, PAGE = 2, 8, 64
+SEGMENT_COST, MIN_PART_PAGES, PAGE = 6, 8, 64
 
 
 def pages_of(L):
