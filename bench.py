@@ -51,6 +51,15 @@ MEASURED_TRAFFIC = {
 }
 
 
+def breakdown_steps(steps: int):
+    """Indices of the timed steps that also carry events between the kernels
+    (every BREAKDOWN_EVERY-th, at least one) and of the plain steps `value`
+    is taken from (all steps if there are no others)."""
+    inner = [k for k in range(steps) if k % BREAKDOWN_EVERY == BREAKDOWN_EVERY - 1] or [steps - 1]
+    plain = [k for k in range(steps) if k not in set(inner)] or list(range(steps))
+    return inner, plain
+
+
 def kernel_digest() -> str:
     """Hash of the decode kernel's sources with // comments and whitespace
     removed: a comment edit keeps the measured traffic, a code edit drops it."""
@@ -219,7 +228,7 @@ def run_ours(args, world, rank, local):
             ev[3].record(stream)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    inner_steps = [k for k in range(args.steps) if k % BREAKDOWN_EVERY == BREAKDOWN_EVERY - 1] or [args.steps - 1]
+    inner_steps, plain = breakdown_steps(args.steps)
     # the clock sampler starts before the warm-up so that its own start-up falls
     # outside the timed loop; only samples taken during the loop are kept
     with ClockSampler(local) as clk:
@@ -244,7 +253,6 @@ def run_ours(args, world, rank, local):
     t_meta = [evs[k][0].elapsed_time(evs[k][1]) for k in inner_steps]
     t_dec = [evs[k][1].elapsed_time(evs[k][2]) for k in inner_steps]
     t_comb = [evs[k][2].elapsed_time(evs[k][3]) for k in inner_steps]
-    plain = [k for k in range(args.steps) if k not in inner_set] or list(range(args.steps))
     t_step = [evs[k][0].elapsed_time(evs[k][3]) for k in plain]
     ms_step = max_over_ranks(float(np.mean(t_step)), world)
     ms_dec = float(np.mean(t_dec))
@@ -277,7 +285,7 @@ def run_ours(args, world, rank, local):
             "num_parts": parts,
             "l2": "flushed between steps by a 512 MB write outside the timed events",
             "step": "metadata + split-KV decode + combine",
-            "timing": f"value from the {args.steps - len(inner_steps)} steps timed with two events each; "
+            "timing": f"value from the {len(plain)} steps timed with two events each; "
                       f"breakdown and roofline from the {len(inner_steps)} steps (every {BREAKDOWN_EVERY}th) "
                       "with events between the kernels",
             "bytes_per_step": nbytes, "flops_per_step": flops,

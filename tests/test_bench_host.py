@@ -1,0 +1,40 @@
+"""Host-side helpers of bench.py: which timed steps carry per-kernel events,
+and the digest that ties a measured ncu traffic figure to the kernel it was
+taken from."""
+import os
+import shutil
+
+import bench
+
+
+def test_breakdown_steps_split_the_timed_steps():
+    inner, plain = bench.breakdown_steps(2000)
+    assert len(inner) == 2000 // bench.BREAKDOWN_EVERY
+    assert not set(inner) & set(plain) and sorted(inner + plain) == list(range(2000))
+    assert all(k % bench.BREAKDOWN_EVERY == bench.BREAKDOWN_EVERY - 1 for k in inner)
+    # too few steps for a breakdown step of their own: the last one carries it,
+    # and a single step serves both
+    assert bench.breakdown_steps(3) == ([2], [0, 1])
+    assert bench.breakdown_steps(1) == ([0], [0])
+
+
+def _copy_sources(tmp_path):
+    src = os.path.join(bench.ROOT, "mla_decode_attention_03_gb300", "csrc")
+    dst = tmp_path / "mla_decode_attention_03_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for name in bench.KERNEL_SOURCES:
+        shutil.copy(os.path.join(src, name), dst / name)
+    return dst
+
+
+def test_kernel_digest_ignores_comments_not_code(tmp_path, monkeypatch):
+    base = bench.kernel_digest()
+    dst = _copy_sources(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_digest() == base
+    f = dst / bench.KERNEL_SOURCES[0]
+    text = f.read_text(encoding="utf-8")
+    f.write_text("// an added comment line\n" + text.replace("\n", "\n  ", 3), encoding="utf-8")
+    assert bench.kernel_digest() == base  # comments and whitespace only
+    f.write_text(text.replace("kStages = 4", "kStages = 3", 1), encoding="utf-8")
+    assert bench.kernel_digest() != base  # a code change
