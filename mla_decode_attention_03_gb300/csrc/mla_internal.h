@@ -13,7 +13,7 @@ constexpr int kPage = 64;       // tokens per cache page
 constexpr int kRowsPerTile = 128;
 constexpr int kMetaInts = 8;    // ints per scheduler part
 constexpr int kSegmentCost = 6; // fixed scheduler cost of one (sequence, part) segment, in pages (measured: 2, 4, 6, 8, 12 -> 6 best)
-constexpr int kMinPartPages = 8;
+constexpr int kMinPartCost = 10;  // smallest part, in cost units (independent of kSegmentCost)
 constexpr int kMaxMetadataBatch = 16384;  // sequences the scheduler stages in shared memory
 
 // Device-side status codes (written to the caller's status word).

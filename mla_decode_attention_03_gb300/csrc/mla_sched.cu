@@ -20,7 +20,7 @@ namespace {
 // Cost axis: sequence i with n_i > 0 pages occupies [C_i, C_i + n_i + F), where
 // C is the exclusive prefix sum of the widths and the first F = kSegmentCost
 // units stand for the fixed cost of a segment (Q load, epilogue).  Part q takes
-// the cost range [q*per, (q+1)*per), per = max(ceil(total/P), F + kMinPartPages).
+// the cost range [q*per, (q+1)*per), per = max(ceil(total/P), kMinPartCost).
 // A cut at cost x falls in sequence i = max{i : C_i <= x}, at page
 // max(0, x - C_i - F); cuts inside a sequence's first F units therefore start
 // the part at that sequence's first page.  Every quantity below is a closed
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
   __syncthreads();
 
   int64_t per = (total + num_parts - 1) / num_parts;
-  if (per < kSegmentCost + kMinPartPages) per = kSegmentCost + kMinPartPages;
+  if (per < kMinPartCost) per = kMinPartCost;
   auto pages = [&](int i) -> int { return static_cast<int>(C[i + 1] - C[i] - kSegmentCost); };
 
   for (int q = tid; q < num_parts; q += kMetaThreads) {

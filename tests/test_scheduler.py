@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-SEGMENT_COST, MIN_PART_PAGES, PAGE = 6, 8, 64
+SEGMENT_COST, MIN_PART_COST, PAGE = 6, 10, 64
 
 
 def pages_of(L):
@@ -30,7 +30,7 @@ def host_schedule(seqlens, parts):
     width = [pages_of(L) + F if pages_of(L) > 0 else 0 for L in seqlens]
     C = np.concatenate([[0], np.cumsum(width)]).astype(np.int64)
     total = int(C[-1])
-    per = max(-(-total // parts), F + MIN_PART_PAGES)
+    per = max(-(-total // parts), MIN_PART_COST)
 
     def seq_at(x):
         return int(np.searchsorted(C[:b], x, side="right")) - 1
@@ -101,7 +101,7 @@ def check_schedule(seqlens, parts, meta, num_splits):
         assert num_splits[i + 1] - num_splits[i] == len(seg_k[i])
     assert num_splits[0] == 0
     total = sum(n + SEGMENT_COST for n in pages if n > 0)
-    per = max(-(-total // parts), SEGMENT_COST + MIN_PART_PAGES)
+    per = max(-(-total // parts), MIN_PART_COST)
     # a part spans at most `per` units of the cost axis, plus the fixed cost of
     # a first segment whose start was paid for by the previous part
     assert max(costs, default=0) <= per + SEGMENT_COST, (max(costs), per)
