@@ -260,6 +260,12 @@ def run_ours(args, world, rank, local):
     # end to end through the public API: pinned host q / block_table / seqlens in,
     # out / lse back, the cache resident in HBM
     e2e = run_e2e(args, w, dev, kc, parts, dec, flush, nbytes)
+    e2e_runs = None
+    if args.e2e_runs:
+        e2e_runs = []
+        for c in (int(x) for x in args.e2e_runs.split(",")):
+            r = run_e2e(args, w, dev, kc, parts, dec, flush, nbytes, chunks=c)
+            e2e_runs.append({"runs": r["runs"], "ms_per_step": r["ms_per_step"], "value": r["value"]})
 
     hbm_peak, tf_peak, peak_src = peaks()
     achieved = nbytes / 1e9 / (ms_dec / 1e3)
@@ -303,6 +309,7 @@ def run_ours(args, world, rank, local):
                      "tensor_tflops_achieved": round(flops / 1e9 / ms_dec, 1),
                      "tensor_frac": round(flops / 1e9 / ms_dec / tf_peak, 4)},
         "e2e": e2e,
+        **({"e2e_runs": e2e_runs} if e2e_runs else {}),
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
@@ -312,7 +319,11 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, w, dev, kc, parts, dec, flush, nbytes):
+def run_e2e(args, w, dev, kc, parts, dec, flush, nbytes, chunks=0):
+    """The same step through the host-buffer entry point (mla_decode_host):
+    q, block_table and cache_seqlens copied in from pinned host memory and
+    out and lse copied back, every step, with the copies of one run of
+    sequences overlapping the decode of its neighbours."""
     from mla_decode_attention_03_gb300 import ops
 
     q_h = w.q.pin_memory()
@@ -320,24 +331,14 @@ def run_e2e(args, w, dev, kc, parts, dec, flush, nbytes):
     sl_h = w.cache_seqlens.pin_memory()
     out_h = torch.empty((w.b, w.s_q, w.h_q, 512), dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty((w.b, w.h_q, w.s_q), dtype=torch.float32).pin_memory()
-    q_d = torch.empty_like(q_h, device=dev)
-    bt_d = torch.empty_like(bt_h, device=dev)
-    sl_d = torch.empty_like(sl_h, device=dev)
-    out_d = torch.empty_like(out_h, device=dev)
-    lse_d = torch.empty_like(lse_h, device=dev)
+    hd = ops.HostDecoder(w.b, w.s_q, w.h_q, bt_h.shape[1], w.h_kv, device=dev, parts=parts)
     stream = torch.cuda.current_stream()
     h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    runs = len(ops.host_chunks(sl_h, chunks)) - 1
 
     def step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        meta, nsplit = ops.get_mla_metadata(sl_d, parts, dec.status)
-        ops.mla_decode_with_kvcache(q_d, kc, bt_d, sl_d, meta, nsplit, w.softmax_scale, w.causal,
-                                    out=out_d, lse=lse_d, workspace=dec.workspace, status=dec.status)
-        out_h.copy_(out_d, non_blocking=True)
-        lse_h.copy_(lse_d, non_blocking=True)
+        hd(q_h, kc, bt_h, sl_h, w.softmax_scale, w.causal, out=out_h, lse=lse_h, chunks=chunks)
 
     for _ in range(3):
         step()
@@ -352,10 +353,13 @@ def run_e2e(args, w, dev, kc, parts, dec, flush, nbytes):
         b.record(stream)
         times.append((a, b))
     torch.cuda.synchronize()
+    ops.check_status(hd.status)
+    hd.close()
     ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
-    return {"value": round(nbytes / 1e6 / ms, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+    return {"value": round(nbytes / 1e6 / ms, 1), "unit": "GB/s", "ms_per_step": round(ms, 5), "runs": runs,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "pinned host q/block_table/seqlens in, out/lse out; the KV cache stays resident"}
+            "note": f"mla_decode_host: pinned host q/block_table/seqlens in, out/lse out, {runs} run(s) of "
+                    "sequences with copies overlapping the decode; the KV cache stays resident"}
 
 
 # ----------------------------------------------------------- CPU baseline
@@ -574,6 +578,9 @@ def main():
                     help="comma-separated mean sequence lengths: print one line per (length, stride)")
     ap.add_argument("--cache-ops", action="store_true",
                     help="time the cache write and copy_blocks kernels instead of the decode step")
+    ap.add_argument("--e2e-runs", default=None,
+                    help="comma-separated run counts: also time the host-buffer step with each "
+                         "(1 = copies in, decode, copies out one after another) and add them as e2e_runs")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

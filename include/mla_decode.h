@@ -248,6 +248,93 @@ mla_status_t mla_decode_with_kvcache_static(const void *q, int b, int s_q, int h
                                             int causal, void *out, float *lse, int32_t *status,
                                             mla_stream_t stream);
 
+/*
+ * Decode from HOST buffers, with the copies overlapped with the compute.
+ * The pages' benchmark hands the decode device tensors; a serving process
+ * whose query vectors and block tables are built on the CPU must also move
+ * them over and read the results back.  This call does the whole round trip:
+ * it cuts the batch into `chunks` runs of consecutive sequences balanced by
+ * their page counts, copies the inputs of run k to the device while run k-1
+ * decodes, and copies the outputs of run k back while run k+1 decodes.  Each
+ * run is an independent, complete decode (its own schedule over all
+ * num_parts clusters), so the results equal those of mla_decode_with_kvcache
+ * up to the rounding of a different split-KV cut (identical with chunks = 1).
+ *
+ * A pipeline object holds two CUDA streams (copies in, copies out) and the
+ * events that order them against the caller's stream; it is the only object
+ * in this library that allocates anything, and only when it is created:
+ *   mla_host_pipeline_create   creates one on the current device (*pipeline
+ *                              receives it; MLA_ERR_CUDA if a stream or event
+ *                              could not be made, nothing is then leaked)
+ *   mla_host_pipeline_destroy  synchronises its streams and frees it (NULL is
+ *                              accepted and ignored)
+ * One pipeline serves one host thread at a time.
+ */
+typedef struct mla_host_pipeline mla_host_pipeline;
+
+#define MLA_HOST_MAX_CHUNKS 8
+
+mla_status_t mla_host_pipeline_create(mla_host_pipeline **pipeline);
+mla_status_t mla_host_pipeline_destroy(mla_host_pipeline *pipeline);
+
+/*
+ * The cut mla_decode_host makes (pure host code, no GPU needed): writes
+ * n + 1 sequence indices 0 = bounds[0] < bounds[1] < ... < bounds[n] = b into
+ * `bounds` (room for MLA_HOST_MAX_CHUNKS + 1) and returns n, or a negative
+ * mla_status_t for b < 1 or NULL pointers.  Sequence i costs
+ * ceil(max(L_i, 0) / 64) + 1 units; run k ends at the first sequence where
+ * the running cost reaches k/n of the total, moved as needed so that every
+ * run holds at least one sequence.  chunks >= 1 asks for that many runs
+ * (capped at MLA_HOST_MAX_CHUNKS and at b); chunks <= 0 picks
+ * n = total pages / 1024 clamped to [1, 4]: fewer, larger runs when the
+ * batch is small, so that the fixed cost of a run (a schedule, a pipeline
+ * fill, a merge) stays small against its pages.
+ */
+int mla_host_chunks(const int32_t *cache_seqlens, int b, int chunks, int32_t *bounds);
+
+/*
+ * Device scratch for mla_decode_host: staging of q, block_table,
+ * cache_seqlens, out and lse for the whole batch, MLA_HOST_MAX_CHUNKS sets of
+ * scheduler metadata and one split-KV workspace, each 256-byte aligned.
+ */
+size_t mla_host_scratch_bytes(int b, int s_q, int h_q, int max_blocks_per_seq, int num_parts);
+
+/*
+ * Arguments as for mla_decode_with_kvcache, except:
+ *   q, block_table, cache_seqlens   HOST arrays (same shapes and types)
+ *   out, lse                        HOST arrays, written
+ *   num_parts                       clusters per run (normally mla_num_parts());
+ *                                   there are no metadata/num_splits arguments:
+ *                                   each run's schedule is made on the device
+ *   chunks                          as for mla_host_chunks
+ *   scratch                         DEVICE memory, >= mla_host_scratch_bytes(...)
+ *                                   bytes, 256-byte aligned, owned by the caller
+ *   kcache, status                  DEVICE, as before
+ * Host memory should be page-locked (cudaHostAlloc / pinned): pageable
+ * buffers give the same results without the overlap.  cache_seqlens is read
+ * by the host during the call (to make the cut) and again by a copy later.
+ * The call returns once everything is enqueued: q, block_table and
+ * cache_seqlens must stay unchanged, and out and lse must not be read, until
+ * `stream` has reached the call's end (e.g. cudaStreamSynchronize(stream)).
+ * All work is ordered after the work already on `stream` and everything
+ * enqueued on `stream` later runs after all of the call's copies.  Calls on
+ * one pipeline are ordered after one another whatever their streams; two
+ * pipelines must not share one scratch buffer while their calls may overlap.
+ * The argument checks of mla_decode_with_kvcache (on the device staging
+ * pointers) run before anything is enqueued; MLA_ERR_INVALID_ARG also for
+ * a NULL pipeline, a pipeline made on another device, a scratch too small or
+ * not 256-byte aligned, and b above 16384.  A CUDA call that fails part-way
+ * returns MLA_ERR_CUDA with the runs before it already enqueued.  Not meant
+ * for stream capture.
+ */
+mla_status_t mla_decode_host(mla_host_pipeline *pipeline, const void *q, int b, int s_q, int h_q,
+                             int d, const void *kcache, int64_t num_blocks, int block_size,
+                             int h_kv, int stride, const int32_t *block_table,
+                             int max_blocks_per_seq, const int32_t *cache_seqlens, int dv,
+                             int num_parts, float softmax_scale, int causal, void *out,
+                             float *lse, int chunks, void *scratch, size_t scratch_bytes,
+                             int32_t *status, mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,7 +15,7 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libmla_decode.so"
-SOURCES = ["mla_decode.cu", "mla_sched.cu", "mla_cache.cu", "mla_api.cu"]
+SOURCES = ["mla_decode.cu", "mla_sched.cu", "mla_cache.cu", "mla_api.cu", "mla_host.cu"]
 HEADERS = ["sm103_ptx.cuh", "mla_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -132,15 +132,14 @@ mla_status_t mla_get_metadata(const int32_t* cache_seqlens, int b, int num_parts
 
 }  // extern "C"
 
-namespace {
+namespace mla {
 
-mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const void* kcache,
-                         int64_t num_blocks, int block_size, int h_kv, int stride,
-                         const int32_t* block_table, int max_blocks_per_seq,
-                         const int32_t* cache_seqlens, int dv, const int32_t* metadata, int num_parts,
-                         const int32_t* num_splits, float softmax_scale, int causal, void* out,
-                         float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
-                         mla_stream_t stream, bool with_combine) {
+int32_t check_decode_args(const void* q, int b, int s_q, int h_q, int d, const void* kcache, int64_t num_blocks,
+                          int block_size, int h_kv, int stride, const int32_t* block_table,
+                          int max_blocks_per_seq, const int32_t* cache_seqlens, int dv,
+                          const int32_t* metadata, int num_parts, const int32_t* num_splits,
+                          float softmax_scale, int causal, const void* out, const float* lse,
+                          const void* workspace, size_t workspace_bytes, const int32_t* status) {
   if (!q || !kcache || !block_table || !cache_seqlens || !metadata || !num_splits || !out || !lse ||
       !workspace || !status)
     return MLA_ERR_INVALID_ARG;
@@ -159,6 +158,25 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
     return MLA_ERR_ALIGNMENT;
   if (workspace_bytes < mla_workspace_bytes(b, s_q, h_q, num_parts)) return MLA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s_q) * h_q > 4 * 65535) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+namespace {
+
+mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const void* kcache,
+                         int64_t num_blocks, int block_size, int h_kv, int stride,
+                         const int32_t* block_table, int max_blocks_per_seq,
+                         const int32_t* cache_seqlens, int dv, const int32_t* metadata, int num_parts,
+                         const int32_t* num_splits, float softmax_scale, int causal, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
+                         mla_stream_t stream, bool with_combine) {
+  const mla_status_t chk = mla::check_decode_args(
+      q, b, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride, block_table, max_blocks_per_seq,
+      cache_seqlens, dv, metadata, num_parts, num_splits, softmax_scale, causal, out, lse, workspace,
+      workspace_bytes, status);
+  if (chk != MLA_OK) return chk;
 
   const Shape s = tile_shape(s_q, h_q, h_kv);
   CUtensorMap q_rope, k_lat, k_rope;

@@ -54,6 +54,16 @@ def load_library():
     lib.mla_write_cache.argtypes = [P, I64, P, I64, P, I64, P, I64, I, I, P, P]
     lib.mla_copy_blocks.restype = ctypes.c_int32
     lib.mla_copy_blocks.argtypes = [P, I, P, I64, I64, I, I, P, P]
+    lib.mla_host_pipeline_create.restype = ctypes.c_int32
+    lib.mla_host_pipeline_create.argtypes = [ctypes.POINTER(P)]
+    lib.mla_host_pipeline_destroy.restype = ctypes.c_int32
+    lib.mla_host_pipeline_destroy.argtypes = [P]
+    lib.mla_host_chunks.restype = I
+    lib.mla_host_chunks.argtypes = [P, I, I, P]
+    lib.mla_host_scratch_bytes.restype = SZ
+    lib.mla_host_scratch_bytes.argtypes = [I, I, I, I, I]
+    lib.mla_decode_host.restype = ctypes.c_int32
+    lib.mla_decode_host.argtypes = [P, P, I, I, I, I, P, I64, I, I, I, P, I, P, I, I, F, I, P, P, I, P, SZ, P, P]
     _lib = lib
     return lib
 
@@ -247,3 +257,92 @@ class MLADecoder:
         return mla_decode_with_kvcache(q, kcache, block_table, cache_seqlens, self.metadata,
                                        self.num_splits, softmax_scale, causal, out=out, lse=lse,
                                        workspace=self.workspace, status=self.status)
+
+
+HOST_MAX_CHUNKS = 8  # MLA_HOST_MAX_CHUNKS
+
+
+def host_chunks(cache_seqlens: torch.Tensor, chunks: int = 0) -> list:
+    """The cut of a batch into runs of consecutive sequences that the
+    host-buffer decode makes (mla_host_chunks): sequence bounds [0, ..., b]."""
+    sl = cache_seqlens.to(torch.int32).contiguous()
+    assert sl.device.type == "cpu" and sl.dim() == 1
+    bounds = (ctypes.c_int32 * (HOST_MAX_CHUNKS + 1))()
+    n = load_library().mla_host_chunks(sl.data_ptr(), sl.shape[0], int(chunks), ctypes.addressof(bounds))
+    if n < 0:
+        _check(n, "mla_host_chunks")
+    return list(bounds[: n + 1])
+
+
+class HostDecoder:
+    """Decode from host tensors (mla_decode_host): q, block_table and
+    cache_seqlens are CPU tensors (pinned for the copies to overlap), out and
+    lse come back in CPU tensors; the KV cache stays on the device.  The batch
+    is cut into runs of sequences whose copies in and out overlap the decode
+    of the neighbouring runs.  Holds the pipeline's streams and events and the
+    device staging scratch for batches up to (b, s_q, h_q, max_blocks_per_seq).
+
+    The call returns once the work is enqueued on the current stream: keep the
+    host tensors alive and unchanged, and read out/lse only after
+    torch.cuda.current_stream().synchronize() (or check_status(self.status))."""
+
+    def __init__(self, b: int, s_q: int, h_q: int, max_blocks_per_seq: int, h_kv: int = 1, device=None,
+                 parts: int | None = None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.b, self.s_q, self.h_q, self.h_kv, self.max_blocks = b, s_q, h_q, h_kv, max_blocks_per_seq
+        self.parts = parts if parts is not None else num_parts(s_q, h_q, h_kv, self.device)
+        lib = load_library()
+        self._handle = None
+        with torch.cuda.device(self.device):
+            h = ctypes.c_void_p()
+            _check(lib.mla_host_pipeline_create(ctypes.byref(h)), "mla_host_pipeline_create")
+            self._handle = h
+        n = lib.mla_host_scratch_bytes(b, s_q, h_q, max_blocks_per_seq, self.parts)
+        if n == 0:
+            raise MLAError("mla_host_scratch_bytes: invalid shape")
+        # zeroed once: no run can ever see stale schedule words, whatever was in the memory before
+        self.scratch = torch.zeros((n,), dtype=torch.uint8, device=self.device)
+        self.status = new_status(self.device)
+
+    def __call__(self, q, kcache, block_table, cache_seqlens, softmax_scale, causal=False, out=None, lse=None,
+                 chunks: int = 0):
+        if self._handle is None:
+            raise MLAError("HostDecoder is closed")
+        for name, t in (("q", q), ("block_table", block_table), ("cache_seqlens", cache_seqlens)):
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise MLAError(f"{name} must be a contiguous CPU tensor")
+        if q.dtype != torch.bfloat16 or kcache.dtype != torch.bfloat16 or not kcache.is_cuda:
+            raise MLAError("q must be bfloat16 on the host and kcache bfloat16 on the device")
+        if block_table.dtype != torch.int32 or cache_seqlens.dtype != torch.int32:
+            raise MLAError("block_table and cache_seqlens must be int32")
+        b, s_q, h_q, d = q.shape
+        if b > self.b or s_q != self.s_q or h_q != self.h_q or block_table.shape[1] > self.max_blocks:
+            raise MLAError(f"shape {tuple(q.shape)} / max_blocks {block_table.shape[1]} outside the decoder's "
+                           f"({self.b}, {self.s_q}, {self.h_q}) / {self.max_blocks}")
+        nb, bs, h_kv, dk = kcache.shape
+        stride = entry_stride(kcache)
+        if out is None:
+            out = torch.empty((b, s_q, h_q, D_V), dtype=torch.bfloat16, pin_memory=True)
+        if lse is None:
+            lse = torch.empty((b, h_q, s_q), dtype=torch.float32, pin_memory=True)
+        if out.device.type != "cpu" or lse.device.type != "cpu" or not (out.is_contiguous() and lse.is_contiguous()):
+            raise MLAError("out and lse must be contiguous CPU tensors")
+        with torch.cuda.device(self.device):
+            rc = load_library().mla_decode_host(
+                self._handle, q.data_ptr(), b, s_q, h_q, d, kcache.data_ptr(), nb, bs, h_kv, stride,
+                block_table.data_ptr(), block_table.shape[1], cache_seqlens.data_ptr(), D_V, self.parts,
+                float(softmax_scale), int(bool(causal)), out.data_ptr(), lse.data_ptr(), int(chunks),
+                self.scratch.data_ptr(), self.scratch.numel(), self.status.data_ptr(), _stream_handle())
+        _check(rc, "mla_decode_host")
+        return out, lse
+
+    def close(self):
+        if self._handle is not None:
+            h, self._handle = self._handle, None
+            _check(load_library().mla_host_pipeline_destroy(h), "mla_host_pipeline_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

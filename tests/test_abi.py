@@ -31,7 +31,9 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "mla_status_string", "mla_num_parts", "mla_metadata_ints", "mla_workspace_bytes",
         "mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits",
-        "mla_decode_with_kvcache_static", "mla_write_cache", "mla_copy_blocks"])
+        "mla_decode_with_kvcache_static", "mla_write_cache", "mla_copy_blocks",
+        "mla_host_pipeline_create", "mla_host_pipeline_destroy", "mla_host_chunks",
+        "mla_host_scratch_bytes", "mla_decode_host"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -95,3 +97,113 @@ def test_sizes_and_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert lib.mla_status_string(code).startswith(b"MLA_")
     assert lib.mla_status_string(12345) == b"MLA: unknown status"
+
+
+# ------------------------------------------------------------ host-buffer pipeline (host logic only)
+MAX_CHUNKS = 8
+
+
+def _chunks(lib, seqlens, chunks):
+    f = lib.mla_host_chunks
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    sl = (ctypes.c_int32 * max(1, len(seqlens)))(*seqlens)
+    bounds = (ctypes.c_int32 * (MAX_CHUNKS + 1))()
+    n = f(ctypes.addressof(sl), len(seqlens), chunks, ctypes.addressof(bounds))
+    return n, list(bounds[: n + 1]) if n > 0 else []
+
+
+def _cost(L):
+    return -(-max(L, 0) // 64) + 1
+
+
+def _check_cut(seqlens, n, bounds):
+    b = len(seqlens)
+    assert bounds[0] == 0 and bounds[-1] == b and len(bounds) == n + 1
+    assert all(x < y for x, y in zip(bounds, bounds[1:])), bounds  # no empty run
+    costs = [_cost(L) for L in seqlens]
+    total = sum(costs)
+    prefix = [0]
+    for c in costs:
+        prefix.append(prefix[-1] + c)
+    for k in range(1, n):
+        e = bounds[k]
+        target = -(-total * k // n)
+        lo, hi = bounds[k - 1] + 1, b - (n - k)
+        if lo < e < hi:
+            # an unclamped bound is the first sequence where the running cost reaches k/n of the total
+            assert prefix[e] >= target and prefix[e - 1] < target, (k, e, target)
+
+
+@pytest.mark.parametrize("seqlens,chunks,want_n", [
+    ([4096] * 128, 4, 4), ([4096] * 128, 0, 4), ([4096] * 128, 1, 1), ([4096] * 128, 8, 8),
+    ([4096] * 128, 100, 8), ([100, 200, 300], 8, 3), ([0, 0, 0, 0], 2, 2), ([5], 3, 1),
+    ([65536, 65536] + [300] * 62, 4, 4), ([65536, 65536] + [300] * 62, 0, 2),
+    ([256] * 16, 0, 1), ([4096] * 16, 0, 1), ([4096] * 32, 0, 2), ([4096] * 64, 0, 4),
+    ([-5, 70, 1, 4096], 2, 2),
+])
+def test_host_chunks_cut(lib, seqlens, chunks, want_n):
+    n, bounds = _chunks(lib, seqlens, chunks)
+    assert n == want_n
+    _check_cut(seqlens, n, bounds)
+
+
+def test_host_chunks_uniform_batch_cuts_evenly(lib):
+    for n_req in (2, 4, 8):
+        n, bounds = _chunks(lib, [4096] * 128, n_req)
+        assert bounds == [128 * k // n_req for k in range(n_req + 1)]
+
+
+def test_host_chunks_random_batches(lib):
+    import random
+    rng = random.Random(7)
+    for _ in range(300):
+        b = rng.randint(1, 40)
+        seqlens = [rng.choice([0, 1, 63, 64, 65, rng.randint(0, 20000)]) for _ in range(b)]
+        chunks = rng.randint(-1, 10)
+        n, bounds = _chunks(lib, seqlens, chunks)
+        pages = sum(-(-max(L, 0) // 64) for L in seqlens)
+        want = min(max(1, min(4, pages // 1024)) if chunks <= 0 else min(chunks, MAX_CHUNKS), b)
+        assert n == want
+        _check_cut(seqlens, n, bounds)
+
+
+def test_host_chunks_rejects_bad_arguments(lib):
+    f = lib.mla_host_chunks
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    assert f(FAKE, 0, 2, FAKE) == -1
+    assert f(None, 4, 2, FAKE) == -1
+    assert f(FAKE, 4, 2, None) == -1
+
+
+def test_host_scratch_bytes(lib):
+    f = lib.mla_host_scratch_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 5
+    lib.mla_workspace_bytes.restype = ctypes.c_size_t
+    lib.mla_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    up = lambda x: (x + 255) // 256 * 256
+    b, s_q, h_q, mb, parts = 128, 1, 128, 64, 76
+    rows = b * s_q * h_q
+    want = (up(rows * 576 * 2) + up(rows * 512 * 2) + up(rows * 4) + up(b * mb * 4) + up(b * 4)
+            + MAX_CHUNKS * up(parts * 8 * 4) + MAX_CHUNKS * up((b + 1) * 4)
+            + lib.mla_workspace_bytes(b, s_q, h_q, parts))
+    assert f(b, s_q, h_q, mb, parts) == want
+    assert f(0, 1, 128, 64, 76) == 0 and f(1, 1, 128, 0, 76) == 0 and f(1, 1, 128, 64, 0) == 0
+
+
+def test_host_decode_rejects_null_pipeline(lib):
+    f = lib.mla_decode_host
+    P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    f.restype = ctypes.c_int32
+    f.argtypes = [P, P, I, I, I, I, P, I64, I, I, I, P, I, P, I, I, F, I, P, P, I, P, SZ, P, P]
+    args = [None, FAKE, 2, 1, 128, 576, FAKE, 10, 64, 1, 576, FAKE, 4, FAKE, 512, 4, 0.04, 0, FAKE, FAKE, 0,
+            FAKE, 1 << 40, FAKE, None]
+    assert f(*args) == -1
+    lib.mla_host_pipeline_destroy.restype = ctypes.c_int32
+    lib.mla_host_pipeline_destroy.argtypes = [P]
+    assert lib.mla_host_pipeline_destroy(None) == 0
+    lib.mla_host_pipeline_create.restype = ctypes.c_int32
+    lib.mla_host_pipeline_create.argtypes = [P]
+    assert lib.mla_host_pipeline_create(None) == -1
