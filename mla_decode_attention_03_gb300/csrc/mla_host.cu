@@ -4,13 +4,14 @@
 // step of the arithmetic is the decode library's own kernels, enqueued per run
 // through the same launch path as mla_decode_with_kvcache.
 //
-// Streams: the caller's stream computes; an internal stream copies inputs in
+// Streams (more than one run): the caller's stream computes; an internal stream copies inputs in
 // (and runs each run's scheduler kernel right behind its copies, so the
 // schedule of run k+1 is made while run k decodes); a second internal stream
 // copies results out.  Events join them:
 //   caller:  rec(start) .. wait(in[k]) decode(k) combine(k) rec(out[k]) .. wait(done)
 //   in:      wait(start) wait(done of the previous call) H2D(k) metadata(k) rec(in[k])
 //   out:     wait(out[k]) D2H(k) .. rec(done)
+// A single run goes entirely on the caller's stream.
 // Runs share one split-KV workspace: run k+1's decode kernel is stream-ordered
 // after run k's combine on the caller's stream.  Each run has its own
 // metadata, because run k+1's schedule is written while run k still reads its
@@ -38,6 +39,8 @@ struct mla_host_pipeline {
   int device;
   cudaStream_t in, out;
   cudaEvent_t start, done;
+  bool has_prev;            // `done` marks the end of an earlier call ...
+  cudaStream_t prev_stream; // ... which was made on this caller stream
   cudaEvent_t in_ready[MLA_HOST_MAX_CHUNKS];
   cudaEvent_t out_ready[MLA_HOST_MAX_CHUNKS];
 };
@@ -219,37 +222,49 @@ mla_status_t mla_decode_host(mla_host_pipeline* pipeline, const void* q, int b, 
     if ((x) != cudaSuccess) return MLA_ERR_CUDA;   \
   } while (0)
 
-  MLA_CUDA(cudaEventRecord(P->start, cs));
-  MLA_CUDA(cudaStreamWaitEvent(P->in, P->start, 0));
-  MLA_CUDA(cudaStreamWaitEvent(P->in, P->done, 0));  // the previous call on this pipeline has finished
-  for (int k = 0; k < n; ++k) {
-    const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
-    MLA_CUDA(cudaMemcpyAsync(q_d + i0 * q_row, qh + i0 * q_row, bk * q_row, cudaMemcpyHostToDevice, P->in));
-    MLA_CUDA(cudaMemcpyAsync(reinterpret_cast<char*>(bt_d) + i0 * bt_row, bth + i0 * bt_row, bk * bt_row,
-                             cudaMemcpyHostToDevice, P->in));
-    MLA_CUDA(cudaMemcpyAsync(sl_d + i0, cache_seqlens + i0, bk * sizeof(int32_t), cudaMemcpyHostToDevice, P->in));
-    const mla_status_t r = mla_get_metadata(sl_d + i0, bk, num_parts, meta_of(k), nsplit_of(k), status, P->in);
-    if (r != MLA_OK) return r;
-    MLA_CUDA(cudaEventRecord(P->in_ready[k], P->in));
+  // One run needs no overlap: copies, schedule, decode and copies back all go
+  // on the caller's stream, without the event hops between streams.
+  const bool split = n > 1;
+  cudaStream_t in_s = split ? P->in : cs;
+  cudaStream_t out_s = split ? P->out : cs;
+  if (split) {
+    MLA_CUDA(cudaEventRecord(P->start, cs));
+    MLA_CUDA(cudaStreamWaitEvent(P->in, P->start, 0));
+    MLA_CUDA(cudaStreamWaitEvent(P->out, P->start, 0));
   }
-  MLA_CUDA(cudaStreamWaitEvent(P->out, P->start, 0));
+  // the previous call on this pipeline has finished (implied by stream order on the same caller stream)
+  if (P->has_prev && P->prev_stream != cs) MLA_CUDA(cudaStreamWaitEvent(in_s, P->done, 0));
   for (int k = 0; k < n; ++k) {
     const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
-    MLA_CUDA(cudaStreamWaitEvent(cs, P->in_ready[k], 0));
+    MLA_CUDA(cudaMemcpyAsync(q_d + i0 * q_row, qh + i0 * q_row, bk * q_row, cudaMemcpyHostToDevice, in_s));
+    MLA_CUDA(cudaMemcpyAsync(reinterpret_cast<char*>(bt_d) + i0 * bt_row, bth + i0 * bt_row, bk * bt_row,
+                             cudaMemcpyHostToDevice, in_s));
+    MLA_CUDA(cudaMemcpyAsync(sl_d + i0, cache_seqlens + i0, bk * sizeof(int32_t), cudaMemcpyHostToDevice, in_s));
+    const mla_status_t r = mla_get_metadata(sl_d + i0, bk, num_parts, meta_of(k), nsplit_of(k), status, in_s);
+    if (r != MLA_OK) return r;
+    if (split) MLA_CUDA(cudaEventRecord(P->in_ready[k], in_s));
+  }
+  for (int k = 0; k < n; ++k) {
+    const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
+    if (split) MLA_CUDA(cudaStreamWaitEvent(cs, P->in_ready[k], 0));
     const mla_status_t r = mla_decode_with_kvcache(
         q_d + i0 * q_row, bk, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride,
         reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(bt_d) + i0 * bt_row), max_blocks_per_seq,
         sl_d + i0, dv, meta_of(k), num_parts, nsplit_of(k), softmax_scale, causal, out_d + i0 * o_row,
         reinterpret_cast<float*>(reinterpret_cast<char*>(lse_d) + i0 * l_row), ws, L.ws_bytes, status, stream);
     if (r != MLA_OK) return r;
-    MLA_CUDA(cudaEventRecord(P->out_ready[k], cs));
-    MLA_CUDA(cudaStreamWaitEvent(P->out, P->out_ready[k], 0));
-    MLA_CUDA(cudaMemcpyAsync(oh + i0 * o_row, out_d + i0 * o_row, bk * o_row, cudaMemcpyDeviceToHost, P->out));
+    if (split) {
+      MLA_CUDA(cudaEventRecord(P->out_ready[k], cs));
+      MLA_CUDA(cudaStreamWaitEvent(P->out, P->out_ready[k], 0));
+    }
+    MLA_CUDA(cudaMemcpyAsync(oh + i0 * o_row, out_d + i0 * o_row, bk * o_row, cudaMemcpyDeviceToHost, out_s));
     MLA_CUDA(cudaMemcpyAsync(lh + i0 * l_row, reinterpret_cast<char*>(lse_d) + i0 * l_row, bk * l_row,
-                             cudaMemcpyDeviceToHost, P->out));
+                             cudaMemcpyDeviceToHost, out_s));
   }
-  MLA_CUDA(cudaEventRecord(P->done, P->out));
-  MLA_CUDA(cudaStreamWaitEvent(cs, P->done, 0));
+  MLA_CUDA(cudaEventRecord(P->done, out_s));
+  if (split) MLA_CUDA(cudaStreamWaitEvent(cs, P->done, 0));
+  P->has_prev = true;
+  P->prev_stream = cs;
 #undef MLA_CUDA
   return MLA_OK;
 }

@@ -50,9 +50,10 @@ def test_several_runs_all_rows(chunks):
 
 
 def test_back_to_back_calls_and_pageable_memory():
-    """Two calls enqueued without a synchronisation between them (the second
-    one's copies in must wait for the first one's decode) give what each
-    gives alone; pageable host tensors give the pinned result."""
+    """Calls enqueued without a synchronisation between them, on one stream
+    and across two (each call's copies in must wait for the previous call's
+    decode and copies out), give what each gives alone; pageable host tensors
+    give the pinned result."""
     w1 = W.make(6, 1, 64, 1, [900, 64, 1, 129, 1000, 333], stride=576, seed=33)
     w2 = W.make(6, 1, 64, 1, [900, 64, 1, 129, 1000, 333], stride=576, seed=34)
     w2 = W.Workload(**{**w2.__dict__, "kcache_alloc": w1.kcache_alloc, "block_table": w1.block_table})
@@ -60,14 +61,20 @@ def test_back_to_back_calls_and_pageable_memory():
     hd = ops.HostDecoder(w1.b, w1.s_q, w1.h_q, w1.block_table.shape[1], w1.h_kv, parts=4)
     a1 = run_host(w1, hd, dev["kcache"], chunks=3)
     a2 = run_host(w2, hd, dev["kcache"], chunks=3)
+    a1_one = run_host(w1, hd, dev["kcache"], chunks=1)
     x1, x2 = host_inputs(w1), host_inputs(w2)
     b1 = hd(*x1[:1], dev["kcache"], *x1[1:], w1.softmax_scale, w1.causal, chunks=3)
     b2 = hd(*x2[:1], dev["kcache"], *x2[1:], w2.softmax_scale, w2.causal, chunks=3)
+    # a one-run call on another stream must still wait for the call before it
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        b3 = hd(*x1[:1], dev["kcache"], *x1[1:], w1.softmax_scale, w1.causal, chunks=1)
+    b4 = hd(*x2[:1], dev["kcache"], *x2[1:], w2.softmax_scale, w2.causal, chunks=3)
     torch.cuda.synchronize()
     ops.check_status(hd.status)
     c2 = run_host(w2, hd, dev["kcache"], chunks=3, pinned=False)
     hd.close()
-    for (o, l), (o_ref, l_ref) in ((b1, a1), (b2, a2), (c2, a2)):
+    for (o, l), (o_ref, l_ref) in ((b1, a1), (b2, a2), (b3, a1_one), (b4, a2), (c2, a2)):
         assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
     assert_matches(w2, *a2, all_rows(w2))
 
