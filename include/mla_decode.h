@@ -27,7 +27,9 @@
  *  - All array pointers are DEVICE pointers on the current CUDA device, owned
  *    by the caller.  The library allocates nothing and never synchronises; the
  *    calls only enqueue kernels on `stream` (a cudaStream_t; NULL = legacy
- *    default stream) and may be captured in a CUDA graph.
+ *    default stream) and may be captured in a CUDA graph.  The host-buffer
+ *    calls at the end of this file (mla_host_*, mla_decode_host) are the one
+ *    exception, and say how.
  *  - bf16 arrays are passed as void* holding IEEE bfloat16 values.
  *  - Arguments that the host can check are checked before anything is
  *    enqueued; a failed check returns a negative mla_status_t and enqueues
