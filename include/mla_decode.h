@@ -325,7 +325,9 @@ size_t mla_host_scratch_bytes(int b, int s_q, int h_q, int max_blocks_per_seq, i
  * The argument checks of mla_decode_with_kvcache (on the device staging
  * pointers) run before anything is enqueued; MLA_ERR_INVALID_ARG also for
  * a NULL pipeline, a pipeline made on another device, a scratch too small or
- * not 256-byte aligned, and b above 16384.  A CUDA call that fails part-way
+ * not 256-byte aligned, b above 16384, and any cache_seqlens entry outside
+ * [0, max_blocks_per_seq*64] (checked on the host, since the lengths are
+ * there).  A CUDA call that fails part-way
  * returns MLA_ERR_CUDA with the runs before it already enqueued.  Not meant
  * for stream capture.
  */

@@ -180,6 +180,12 @@ mla_status_t mla_decode_host(mla_host_pipeline* pipeline, const void* q, int b, 
   if (reinterpret_cast<uintptr_t>(scratch) & 255u) return MLA_ERR_INVALID_ARG;
   const Layout L = layout(b, s_q, h_q, max_blocks_per_seq, num_parts);
   if (scratch_bytes < L.total) return MLA_ERR_INVALID_ARG;
+  // The lengths are on the host here, so the range the device-buffer call can
+  // only report (L < 0) or cannot see at all (L above the table's width) is
+  // rejected before anything is enqueued.
+  const int64_t max_len = static_cast<int64_t>(max_blocks_per_seq) * mla::kPage;
+  for (int i = 0; i < b; ++i)
+    if (cache_seqlens[i] < 0 || cache_seqlens[i] > max_len) return MLA_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
   if (dev != pipeline->device) return MLA_ERR_INVALID_ARG;

@@ -193,6 +193,25 @@ def test_host_scratch_bytes(lib):
     assert f(0, 1, 128, 64, 76) == 0 and f(1, 1, 128, 0, 76) == 0 and f(1, 1, 128, 64, 0) == 0
 
 
+def test_host_decode_checks_lengths_on_the_host(lib):
+    """Lengths outside [0, max_blocks*64] are rejected before any CUDA call
+    (the pipeline pointer is never dereferenced on that path); a length at the
+    limit passes the check and only then needs the GPU (MLA_ERR_CUDA here)."""
+    f = lib.mla_decode_host
+    P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    f.restype = ctypes.c_int32
+    f.argtypes = [P, P, I, I, I, I, P, I64, I, I, I, P, I, P, I, I, F, I, P, P, I, P, SZ, P, P]
+
+    def call(seqlens):
+        sl = (ctypes.c_int32 * len(seqlens))(*seqlens)
+        return f(FAKE, FAKE, len(seqlens), 1, 128, 576, FAKE, 10, 64, 1, 576, FAKE, 4, ctypes.addressof(sl),
+                 512, 4, 0.04, 0, FAKE, FAKE, 0, FAKE, 1 << 40, FAKE, None)
+
+    assert call([256, -1]) == -1
+    assert call([257, 5]) == -1
+    assert call([256, 0, 17]) == -4
+
+
 def test_host_decode_rejects_null_pipeline(lib):
     f = lib.mla_decode_host
     P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
