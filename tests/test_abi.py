@@ -226,3 +226,19 @@ def test_host_decode_rejects_null_pipeline(lib):
     lib.mla_host_pipeline_create.restype = ctypes.c_int32
     lib.mla_host_pipeline_create.argtypes = [P]
     assert lib.mla_host_pipeline_create(None) == -1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No CPU fallback: with the CUDA library missing, the binding raises
+    instead of computing anything."""
+    import torch
+
+    from mla_decode_attention_03_gb300 import ops
+    monkeypatch.setattr(ops, "LIB_PATH", tmp_path / "libmla_decode.so")
+    monkeypatch.setattr(ops, "_lib", None)
+    with pytest.raises(ops.MLAError, match="missing"):
+        ops.load_library()
+    with pytest.raises(ops.MLAError):
+        ops.workspace_bytes(1, 1, 128, 4)
+    with pytest.raises(ops.MLAError):
+        ops.host_chunks(torch.tensor([64, 128], dtype=torch.int32))
