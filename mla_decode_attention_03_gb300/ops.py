@@ -130,6 +130,29 @@ def entry_stride(kcache: torch.Tensor) -> int:
     return es
 
 
+def _check_io(q, block_table, cache_seqlens, out, lse, dv=D_V):
+    """Shapes, types and layouts of the per-sequence arrays against q
+    [b, s_q, h_q, d]: the library reads and writes exactly these extents, so a
+    smaller tensor must be refused here, before its pointer is handed over."""
+    if q.dim() != 4:
+        raise MLAError(f"q must be [b, s_q, h_q, d], got shape {tuple(q.shape)}")
+    b, s_q, h_q, _ = q.shape
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != b:
+        raise MLAError(f"block_table must be int32 [{b}, max_blocks], got {block_table.dtype} "
+                       f"{tuple(block_table.shape)}")
+    if cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (b,):
+        raise MLAError(f"cache_seqlens must be int32 [{b}], got {cache_seqlens.dtype} {tuple(cache_seqlens.shape)}")
+    for name, t, shape, dtype in (("out", out, (b, s_q, h_q, dv), torch.bfloat16),
+                                  ("lse", lse, (b, h_q, s_q), torch.float32)):
+        if t is None:
+            continue
+        if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous():
+            raise MLAError(f"{name} must be a contiguous {dtype} tensor of shape {shape}, got {t.dtype} "
+                           f"{tuple(t.shape)}{'' if t.is_contiguous() else ' (not contiguous)'}")
+        if t.device != q.device:
+            raise MLAError(f"{name} must be on {q.device}")
+
+
 def mla_decode_with_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
                             cache_seqlens: torch.Tensor, metadata: torch.Tensor,
                             num_splits: torch.Tensor, softmax_scale: float, causal: bool = False,
@@ -146,12 +169,16 @@ def mla_decode_with_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: 
         raise MLAError("q and kcache must be bfloat16")
     if not q.is_contiguous():
         raise MLAError("q must be contiguous")
+    _check_io(q, block_table, cache_seqlens, out, lse, dv)
     b, s_q, h_q, d = q.shape
     nb, bs, h_kv, dk = kcache.shape
     stride = entry_stride(kcache)
     bt = block_table.contiguous()
     sl = cache_seqlens.contiguous()
-    assert bt.dtype == torch.int32 and sl.dtype == torch.int32 and bt.shape[0] == b
+    if not (bt.device == sl.device == kcache.device == q.device):
+        raise MLAError("q, kcache, block_table and cache_seqlens must be on one device")
+    if tuple(num_splits.shape) != (b + 1,) or metadata.dim() != 2 or metadata.shape[1] != 8:
+        raise MLAError("metadata / num_splits do not come from get_mla_metadata for this batch")
     parts = metadata.shape[0]
     dev = q.device
     if out is None:
@@ -178,7 +205,16 @@ def mla_decode_with_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: 
 def combine_splits(num_splits: torch.Tensor, workspace: torch.Tensor, parts: int, out: torch.Tensor,
                    lse: torch.Tensor):
     """The merge half of mla_decode_with_kvcache (mla_combine_splits)."""
+    if out.dim() != 4 or out.shape[3] != D_V or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise MLAError(f"out must be a contiguous bfloat16 [b, s_q, h_q, {D_V}] tensor")
     b, s_q, h_q, _ = out.shape
+    if (tuple(lse.shape) != (b, h_q, s_q) or lse.dtype != torch.float32 or not lse.is_contiguous()
+            or lse.device != out.device):
+        raise MLAError(f"lse must be a contiguous float32 [{b}, {h_q}, {s_q}] tensor on {out.device}")
+    if tuple(num_splits.shape) != (b + 1,):
+        raise MLAError(f"num_splits must have {b + 1} entries")
+    if workspace.numel() * workspace.element_size() < workspace_bytes(b, s_q, h_q, parts):
+        raise MLAError("workspace smaller than mla_workspace_bytes for this shape")
     _check(load_library().mla_combine_splits(num_splits.data_ptr(), b, s_q, h_q, workspace.data_ptr(),
                                              parts, out.data_ptr(), lse.data_ptr(), _stream_handle()),
            "mla_combine_splits")
@@ -226,6 +262,8 @@ def copy_blocks(kcaches: list, block_mapping: torch.Tensor, status: torch.Tensor
     dev = kcaches[0].device
     ptrs = torch.tensor([c.data_ptr() for c in kcaches], dtype=torch.int64, device=dev)
     bm = block_mapping.to(device=dev, dtype=torch.int64).contiguous()
+    if bm.dim() != 2 or bm.shape[1] != 2:
+        raise MLAError(f"block_mapping must be [num_pairs, 2], got {tuple(bm.shape)}")
     if status is None:
         status = new_status(dev)
     _check(load_library().mla_copy_blocks(ptrs.data_ptr(), len(kcaches), bm.data_ptr(), bm.shape[0], nb, bs,
@@ -315,6 +353,7 @@ class HostDecoder:
             raise MLAError("q must be bfloat16 on the host and kcache bfloat16 on the device")
         if block_table.dtype != torch.int32 or cache_seqlens.dtype != torch.int32:
             raise MLAError("block_table and cache_seqlens must be int32")
+        _check_io(q, block_table, cache_seqlens, out, lse)
         b, s_q, h_q, d = q.shape
         if b > self.b or s_q != self.s_q or h_q != self.h_q or block_table.shape[1] > self.max_blocks:
             raise MLAError(f"shape {tuple(q.shape)} / max_blocks {block_table.shape[1]} outside the decoder's "

@@ -242,3 +242,70 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
         ops.workspace_bytes(1, 1, 128, 4)
     with pytest.raises(ops.MLAError):
         ops.host_chunks(torch.tensor([64, 128], dtype=torch.int32))
+
+
+# ------------------------------------------------------------ binding argument checks (no GPU reached)
+def _io(b=4, s_q=1, h_q=128, mb=8):
+    import torch
+    return dict(q=torch.empty((b, s_q, h_q, 576), dtype=torch.bfloat16),
+                block_table=torch.empty((b, mb), dtype=torch.int32),
+                cache_seqlens=torch.empty((b,), dtype=torch.int32),
+                out=torch.empty((b, s_q, h_q, 512), dtype=torch.bfloat16),
+                lse=torch.empty((b, h_q, s_q), dtype=torch.float32))
+
+
+@pytest.mark.parametrize("b,s_q,h_q,mb", [(128, 1, 128, 64), (128, 2, 128, 100), (6, 1, 128, 64), (1, 1, 16, 4),
+                                          (16, 1, 16, 64), (9, 2, 128, 48), (6, 1, 64, 16)])
+def test_check_io_accepts_the_shapes_the_library_is_called_with(b, s_q, h_q, mb):
+    from mla_decode_attention_03_gb300 import ops
+    a = _io(b, s_q, h_q, mb)
+    ops._check_io(**a)
+    ops._check_io(a["q"], a["block_table"], a["cache_seqlens"], None, None)
+
+
+def test_check_io_refuses_what_would_be_read_or_written_out_of_bounds():
+    import torch
+
+    from mla_decode_attention_03_gb300 import ops
+    bad = [
+        ("block_table", torch.empty((3, 8), dtype=torch.int32)),        # fewer rows than sequences
+        ("block_table", torch.empty((4, 8), dtype=torch.int64)),
+        ("block_table", torch.empty((32,), dtype=torch.int32)),
+        ("cache_seqlens", torch.empty((3,), dtype=torch.int32)),
+        ("cache_seqlens", torch.empty((4, 1), dtype=torch.int32)),
+        ("cache_seqlens", torch.empty((4,), dtype=torch.int64)),
+        ("out", torch.empty((4, 1, 64, 512), dtype=torch.bfloat16)),    # too small
+        ("out", torch.empty((4, 1, 128, 512), dtype=torch.float16)),
+        ("out", torch.empty((4, 1, 512, 128), dtype=torch.bfloat16).transpose(2, 3)),  # not contiguous
+        ("lse", torch.empty((4, 1, 128), dtype=torch.float32)),         # [b, s_q, h_q] instead of [b, h_q, s_q]
+        ("lse", torch.empty((4, 128, 1), dtype=torch.float64)),
+    ]
+    for name, t in bad:
+        a = _io()
+        a[name] = t
+        with pytest.raises(ops.MLAError):
+            ops._check_io(**a)
+    a = _io()
+    a["q"] = a["q"][0]
+    with pytest.raises(ops.MLAError):
+        ops._check_io(**a)
+
+
+def test_combine_and_copy_blocks_refuse_bad_shapes_before_the_library():
+    import torch
+
+    from mla_decode_attention_03_gb300 import ops
+    a = _io()
+    ns = torch.empty((5,), dtype=torch.int32)
+    ws = torch.empty((1 << 20,), dtype=torch.uint8)
+    with pytest.raises(ops.MLAError):
+        ops.combine_splits(ns, ws, 4, a["out"], torch.empty((4, 1, 128), dtype=torch.float32))
+    with pytest.raises(ops.MLAError):
+        ops.combine_splits(torch.empty((4,), dtype=torch.int32), ws, 4, a["out"], a["lse"])
+    with pytest.raises(ops.MLAError):
+        ops.combine_splits(ns, torch.empty((16,), dtype=torch.uint8), 4, a["out"], a["lse"])
+    with pytest.raises(ops.MLAError):
+        ops.combine_splits(ns, ws, 4, a["out"][..., :256], a["lse"])
+    cache = torch.empty((4, 64, 1, 576), dtype=torch.bfloat16)
+    with pytest.raises(ops.MLAError, match="num_pairs, 2"):
+        ops.copy_blocks([cache], torch.tensor([0, 1, 2, 3]))
