@@ -83,7 +83,7 @@ size_t mla_metadata_ints(int num_parts);
 
 /*
  * Bytes of scratch the decode call needs for split partial results:
- * (b + num_parts) x s_q x h_q x 512 bf16 partial outputs, then
+ * (b + num_parts) x s_q x h_q x 512 fp32 partial outputs, then
  * (b + num_parts) x s_q x h_q fp32 partial lse, each block 256-byte aligned.
  */
 size_t mla_workspace_bytes(int b, int s_q, int h_q, int num_parts);
@@ -147,7 +147,7 @@ mla_status_t mla_decode_with_kvcache(const void *q, int b, int s_q, int h_q, int
  * schedule them separately.  mla_decode_splitkv takes the same arguments and
  * runs only the decode kernel: sequences cut into one piece get their out and
  * lse written directly; the pieces of the others go to `workspace` as
- * normalised bf16 partial outputs and fp32 natural-log partial lse.
+ * normalised fp32 partial outputs and fp32 natural-log partial lse.
  * mla_combine_splits then merges those pieces by their log-sum-exps (the
  * Flash-Decoding merge) into out and lse, and writes out = 0, lse = -inf for
  * sequences of length 0.  It must run after mla_decode_splitkv on the same
@@ -218,10 +218,10 @@ mla_status_t mla_copy_blocks(const uint64_t *kcaches, int num_layers, const int6
  * beyond its inputs and outputs.  The pages have no counterpart of this call.
  *
  * It exists for callers that have no way to obtain device memory of their
- * own at the point of the call: code running while a CUDA stream is being
- * captured into a graph (where cudaMalloc is not allowed), or code loaded into
- * a host program whose device memory is entirely owned by that program's pool
- * and which gives its plug-ins no allocator.
+ * own at the point of the call: code loaded into a host program whose device
+ * memory is entirely owned by that program's pool and which gives its
+ * plug-ins no allocator, or a latency-critical serving loop that must not
+ * call cudaMalloc, which can synchronise the whole device.
  *
  * Limits and behaviour:
  *  - Every process that loads the library keeps the 64 MiB buffer on each GPU
@@ -231,8 +231,10 @@ mla_status_t mla_copy_blocks(const uint64_t *kcaches, int num_layers, const int6
  *    before anything is enqueued (b=128, s_q=1, h_q=128 with 76 parts needs
  *    about 54 MB and fits).
  *  - The first call on a device looks the buffer's device address up
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before starting any stream capture.
+ *    (cudaGetSymbolAddress) with that device current and keeps it for the
+ *    life of the process.  The address belongs to the device's primary
+ *    context: after cudaDeviceReset, or with another context current on that
+ *    device, it is no longer valid and the call must not be used.
  *  - All calls share the one buffer: calls whose kernels may overlap on the
  *    GPU (different streams without ordering, or several host threads) race
  *    on it and give undefined results.  Calls ordered on one stream are safe.

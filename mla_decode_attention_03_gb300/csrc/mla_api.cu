@@ -48,7 +48,7 @@ Shape tile_shape(int s_q, int h_q, int h_kv) {
 
 size_t workspace_o_bytes(int b, int s_q, int h_q, int num_parts) {
   const size_t slots = static_cast<size_t>(b) + static_cast<size_t>(num_parts);
-  const size_t bytes = slots * static_cast<size_t>(s_q) * h_q * kDimV * 2;  // bf16 partials
+  const size_t bytes = slots * static_cast<size_t>(s_q) * h_q * kDimV * 4;  // fp32 partials
   return (bytes + 255) & ~static_cast<size_t>(255);
 }
 

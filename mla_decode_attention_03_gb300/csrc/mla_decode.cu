@@ -69,11 +69,14 @@ constexpr int kFirstSoftmaxWarp = 8;
 constexpr uint32_t kRegsIssue = 48;
 constexpr uint32_t kRegsStage = 120;
 constexpr uint32_t kRegsSoftmax = 168;
-constexpr int kStages = 4;
+// A K stage is held from its TMA issue (about 1.3 us of HBM latency under
+// load) until the PV of its page has read V, so the number of stages bounds the
+// pages in flight; five stages and a single exchange slot fill the 227 KB.
+constexpr int kStages = 5;
 constexpr int kKChunk = kPage * 128;           // 64 tokens x 64 dims bf16 (128B swizzle)
 constexpr int kKRope = kPage * 64;             // 64 tokens x 32 dims bf16 (64B swizzle)
 constexpr int kKStage = 4 * kKChunk + kKRope;  // 36864 bytes: this CTA's 288 dims of a page
-constexpr int kXSlots = 2;     // receive slots (peer partials)
+constexpr int kXSlots = 1;     // receive slots (peer partials)
 constexpr int kXData = kRowsPerTile * 128;     // 128 rows x 64 int16 (two 32-token halves)
 constexpr int kXSlot = kXData + 2 * kRowsPerTile * 4;  // + one fp32 scale per (row, half)
 constexpr int kQRope = kRowsPerTile * 64;      // Q rope quarter: 128 rows x 32 bf16 (64B swizzle)
@@ -96,12 +99,20 @@ constexpr int kBarPFull = kBarSFree + 2;
 constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
 constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: the peer has read the slot
-constexpr int kBarPVIssued = kBarXEmpty + kXSlots;  // 2: PV of a page (by parity) has been issued
-constexpr int kBarDone = kBarPVIssued + 2;
+// PV of page n has been issued, one barrier per page mod 4.  QK(n) waits for
+// PV(n-3); PV(n+1) -- the next page on the same barrier -- cannot be issued
+// before QK(n) (its softmax needs S(n) first), so the barrier is never two
+// phases ahead of that wait.  With two barriers (page parity) PV(n-3) and
+// PV(n-1) could both be issued while QK(n) waited for its K page, and the
+// parity wait would then hang until PV(n+1).
+constexpr int kPVIssuedBars = 4;
+constexpr int kBarPVIssued = kBarXEmpty + kXSlots;
+constexpr int kBarDone = kBarPVIssued + kPVIssuedBars;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffMisc + 16 + 4 * kXSlots;  // tmem slot, abort flag, pad, slot-read counters
+constexpr int kOffLoFlag = kOffMisc + 16 + 4 * kXSlots;  // two words: page (by parity) + 1 when its low part runs
+constexpr int kSmemUsed = kOffLoFlag + 8;  // tmem slot, abort flag, pad, slot-read counters, low-part flags
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kOffQL % 1024 == 0, "Q latent tile must sit on a 128B-swizzle atom");
 static_assert(kOffQR % 512 == 0, "Q rope tile must sit on a 64B-swizzle atom");
@@ -117,6 +128,12 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// A page gets a second PV pass with the bf16 rounding error of P (P - bf16(P),
+// itself in bf16) when one of its weights exceeds a quarter of the running sum
+// of its row half: 3 * e > l_prev.  Such weights carry enough of the output
+// that the 2^-9 relative rounding of P alone could move an output element by
+// more than the tolerance when value rows cancel.
+constexpr float kLoRatio = 3.0f;
 constexpr float kQuantMax = 32767.0f;
 // q in [-32767, 32767] travels as the low 16 bits of the fp32 value
 // 1.5*2^23 + 32768 + q, whose unit in the last place is 1: one FMA rounds and
@@ -216,6 +233,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + kOffMisc + 4);
   uint32_t* const xread_cnt = reinterpret_cast<uint32_t*>(gbase + kOffMisc + 16);  // [kXSlots]
+  volatile int* const lo_flag = reinterpret_cast<volatile int*>(gbase + kOffLoFlag);  // [2]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -232,6 +250,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < kXSlots; ++s) xread_cnt[s] = 0;
+    lo_flag[0] = 0;
+    lo_flag[1] = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
@@ -243,8 +263,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarSFree + s), 8 + 4);  // softmax warps + sender warps
     }
     mbar_init(bar(kBarPFull), 8);
-    mbar_init(bar(kBarPVIssued), 1);
-    mbar_init(bar(kBarPVIssued + 1), 1);
+    for (int s = 0; s < kPVIssuedBars; ++s) mbar_init(bar(kBarPVIssued + s), 1);
     mbar_init(bar(kBarOFull), 1);
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(bar(kBarXFull + s), 1);
@@ -361,11 +380,12 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       const uint64_t d_v = smem_desc(base + kOffK, kKChunk, 1024, kSwizzle128B);
       PageWalk wp;
       wp.start(meta, P.cache_seqlens, P.max_blocks);
-      int np = 0;
+      int np = 0, kp = 0;  // pages, P hand-offs
       bool ok = true;
       while (wp.valid) {
-        ok = mbar_wait(bar(kBarPFull), np & 1, abort_flag);
+        ok = mbar_wait(bar(kBarPFull), kp & 1, abort_flag);
         if (!ok) break;
+        ++kp;
         tc_fence_after_sync();
         const int st = np % kStages;
         const uint64_t voff = static_cast<uint64_t>((st * kKStage) >> 4);
@@ -375,9 +395,24 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
                        d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV,
                        (first && ks == 0) ? 0u : 1u);
-        umma_commit(bar(kBarEmpty + st));
+        // the softmax warps asked for the low part of this page's P (visible:
+        // written before their arrivals on the barrier just waited on)
+        const bool lo = (lo_flag[np & 1] == np + 1);
+        if (!lo) umma_commit(bar(kBarEmpty + st));
         umma_commit(bar(kBarOFull));
-        mbar_arrive(bar(kBarPVIssued + (np & 1)));
+        mbar_arrive(bar(kBarPVIssued + (np % kPVIssuedBars)));
+        if (lo) {
+          ok = mbar_wait(bar(kBarPFull), kp & 1, abort_flag);
+          if (!ok) break;
+          ++kp;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
+                         d_v + voff + static_cast<uint64_t>((ks * 2048) >> 4), kIdescPV, 1u);
+          umma_commit(bar(kBarEmpty + st));
+          umma_commit(bar(kBarOFull));
+        }
         ++np;
         wp.advance();
       }
@@ -417,7 +452,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
             if (!ok) break;
           }
           if (n >= 3) {
-            ok = mbar_wait(bar(kBarPVIssued + ((n - 3) & 1)), ((n - 3) >> 1) & 1, abort_flag);
+            ok = mbar_wait(bar(kBarPVIssued + ((n - 3) % kPVIssuedBars)), ((n - 3) / kPVIssuedBars) & 1, abort_flag);
             if (!ok) break;
           }
           const int st = n % kStages;
@@ -495,185 +530,208 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const float c_log2 = P.scale_log2;
     const float rescale_raw = kRescaleThreshold / c_log2;
 
-    // wa walks the page being sent (n), wb the page being finished (n - 1).
-    PageWalk wa, wb;
-    wa.start(meta, P.cache_seqlens, P.max_blocks);
-    wb.valid = false;
+    PageWalk w;
+    w.start(meta, P.cache_seqlens, P.max_blocks);
     float m_run = -INFINITY, l_run = 0.f;
-    int lim_a = 0, lim_b = 0;
+    int lim = 0;
     int n = 0;
+    int groups = 0;  // P hand-offs to the PV warp so far (two on pages with a low-part pass)
     bool ok = true;
-    float a_prev[32];
-    while (ok && (wa.valid || wb.valid)) {
-      float a_cur[32];
-      if (wa.valid) {
-        // ======== page n: own partial out of tensor memory (the sender warps
-        // quantise and send the same partial to the peer)
-        if (wa.first()) {
-          const int L = __ldg(P.cache_seqlens + wa.i);
-          lim_a = min(P.causal ? L - P.s_q + j + 1 : L, L);
-        }
-        const int sb = n & 1;
-        const int slot = n % kXSlots;
-        if (leader) mbar_arrive_expect_tx(bar(kBarXFull + slot), kXSlot);
-        ok = mbar_wait(bar(kBarSFull + sb), (n >> 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after_sync();
-        {
-          uint32_t s[32];
-          tmem_ld16x2_32(tmem + lane_off + kTmemS + 64u * sb, s);
-          tmem_wait_ld(s);
+    while (ok && w.valid) {
+      if (w.first()) {
+        const int L = __ldg(P.cache_seqlens + w.i);
+        lim = min(P.causal ? L - P.s_q + j + 1 : L, L);
+        m_run = -INFINITY;
+        l_run = 0.f;
+      }
+      // ======== page n: own partial S out of tensor memory (the sender warps
+      // quantise and send the same partial to the peer meanwhile)
+      const int sb = n & 1;
+      const int slot = n % kXSlots;
+      if (leader) mbar_arrive_expect_tx(bar(kBarXFull + slot), kXSlot);
+      ok = mbar_wait(bar(kBarSFull + sb), (n >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after_sync();
+      float x[32];
+      {
+        uint32_t s[32];
+        tmem_ld16x2_32(tmem + lane_off + kTmemS + 64u * sb, s);
+        tmem_wait_ld(s);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) a_cur[c] = __uint_as_float(s[c]);
+        for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(s[c]);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSFree + sb));
+
+      // ======== add the peer's partial
+      ok = mbar_wait(bar(kBarXFull + slot), (n / kXSlots) & 1, abort_flag);
+      if (!ok) break;
+      {
+        const uint8_t* xr = gbase + kOffX + slot * kXSlot;
+        const float sc = *reinterpret_cast<const float*>(xr + x_scale(sw, lane_i));
+        const uint64_t sc2 = f2(sc, sc), nbase2 = f2(-kQuantBase, -kQuantBase);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + x_chunk(sw, lane_i, k));
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * k + 2 * e;
+            const uint64_t q = f2_add(f2(__uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7610)),
+                                         __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7632))),
+                                      nbase2);
+            f2_split(f2_fma(q, sc2, f2(x[c], x[c + 1])), x[c], x[c + 1]);
+          }
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSFree + sb));
+      }
+      // The slot has been read: the last of the 8 softmax warps to finish
+      // returns it to the peer's senders.  Each warp's fence orders its lanes'
+      // loads (after the warp barrier) before its count; the last warp's fence
+      // orders all of them before its remote arrive.
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        if (atomicAdd(xread_cnt + slot, 1u) == 7u) {
+          xread_cnt[slot] = 0u;
+          __threadfence_block();
+          mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(slot));
+        }
       }
 
-      if (wb.valid) {
-        // ======== page n - 1: add the peer's partial, online softmax, P
-        const int nb = n - 1;
-        const int slot = nb % kXSlots;
-        if (wb.first()) {
-          m_run = -INFINITY;
-          l_run = 0.f;
+      // ======== online softmax
+      const int t0 = w.p * kPage + tok0;
+      if (t0 + 32 > lim) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (t0 + c >= lim) x[c] = -INFINITY;
+      }
+      float mx4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx4[u] = x[u];
+#pragma unroll
+      for (int c = 4; c < 28; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx4[u] = fmax3(mx4[u], x[c + u], x[c + 4 + u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx4[u] = fmaxf(mx4[u], x[28 + u]);
+      const float mx_lane = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+      const float mx = fmaxf(mx_lane, __shfl_xor_sync(0xffffffffu, mx_lane, 16));  // the row's other 32 tokens
+      float alpha = 1.f;
+      {
+        const float m_new = fmaxf(m_run, mx);
+        if (m_new > m_run + rescale_raw) {
+          alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
+          m_run = m_new;
         }
-        ok = mbar_wait(bar(kBarXFull + slot), (nb / kXSlots) & 1, abort_flag);
+      }
+      const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
+      // Does a weight of this warp's lanes exceed a quarter of its running sum?
+      // (-inf lanes give 0, NaN compares false.)
+      const bool want_lo = __any_sync(0xffffffffu, ex2_approx(fmaf(mx_lane, c_log2, neg_mc)) * kLoRatio > l_run * alpha);
+      uint32_t pk[16], lo[16];
+      float rsum;
+      {
+        const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc), neg1 = f2(-1.f, -1.f);
+        uint64_t sum2[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float a0, a1;
+          f2_split(f2_fma(f2(x[2 * c], x[2 * c + 1]), c2, nmc2), a0, a1);
+          const float e0 = ex2_approx(a0);
+          const float e1 = ex2_approx(a1);
+          sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
+          pk[c] = pack_bf16x2(e0, e1);
+          if (want_lo) {
+            // the bf16 rounding error of the pair, itself rounded to bf16
+            float r0, r1;
+            f2_split(f2_fma(f2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)), neg1,
+                            f2(e0, e1)),
+                     r0, r1);
+            lo[c] = pack_bf16x2(r0, r1);
+          } else {
+            lo[c] = 0u;
+          }
+        }
+        float sum8[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f2_split(sum2[u], sum8[2 * u], sum8[2 * u + 1]);
+        rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      }
+      l_run = l_run * alpha + rsum;  // this lane's 32 tokens; the row sum adds lane l^16's
+      // Every PV issued so far must be complete: it read the P buffer, and O
+      // is rescaled below.
+      if (groups > 0) {
+        ok = mbar_wait(bar(kBarOFull), (groups - 1) & 1, abort_flag);
         if (!ok) break;
-        float x[32];
-        {
-          const uint8_t* xr = gbase + kOffX + slot * kXSlot;
-          const float sc = *reinterpret_cast<const float*>(xr + x_scale(sw, lane_i));
-          const uint64_t sc2 = f2(sc, sc), nbase2 = f2(-kQuantBase, -kQuantBase);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xr + x_chunk(sw, lane_i, k));
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 8 * k + 2 * e;
-              const uint64_t q = f2_add(f2(__uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7610)),
-                                           __uint_as_float(__byte_perm(wv[e], kQuantHi, 0x7632))),
-                                        nbase2);
-              f2_split(f2_fma(q, sc2, f2(a_prev[c], a_prev[c + 1])), x[c], x[c + 1]);
-            }
-          }
-        }
-        // The slot has been read: the last of the 8 softmax warps to finish
-        // returns it to the peer's senders.  Each warp's fence orders its lanes'
-        // loads (after the warp barrier) before its count; the last warp's fence
-        // orders all of them before its remote arrive.
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence_block();
-          if (atomicAdd(xread_cnt + slot, 1u) == 7u) {
-            xread_cnt[slot] = 0u;
-            __threadfence_block();
-            mbar_arrive_cluster_relaxed(peer_xempty + 8u * static_cast<uint32_t>(slot));
-          }
-        }
-        const int t0 = wb.p * kPage + tok0;
-        if (t0 + 32 > lim_b) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (t0 + c >= lim_b) x[c] = -INFINITY;
-        }
-        float mx4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) mx4[u] = x[u];
-#pragma unroll
-        for (int c = 4; c < 28; c += 8) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) mx4[u] = fmax3(mx4[u], x[c + u], x[c + 4 + u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) mx4[u] = fmaxf(mx4[u], x[28 + u]);
-        float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the row's other 32 tokens
-        float alpha = 1.f;
-        {
-          const float m_new = fmaxf(m_run, mx);
-          if (m_new > m_run + rescale_raw) {
-            alpha = ex2_approx((m_run - m_new) * c_log2);  // 0 when m_run = -inf
-            m_run = m_new;
-          }
-        }
-        uint32_t pk[16];
-        float rsum;
-        {
-          const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
-          const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
-          uint64_t sum2[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            float a0, a1;
-            f2_split(f2_fma(f2(x[2 * c], x[2 * c + 1]), c2, nmc2), a0, a1);
-            const float e0 = ex2_approx(a0);
-            const float e1 = ex2_approx(a1);
-            sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
-            pk[c] = pack_bf16x2(e0, e1);
-          }
-          float sum8[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) f2_split(sum2[u], sum8[2 * u], sum8[2 * u + 1]);
-          rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        }
-        l_run = l_run * alpha + rsum;  // this lane's 32 tokens; the row sum adds lane l^16's
-        // PV of the previous page has to be complete: it read the P buffer, and O
-        // is rescaled below.
-        if (nb >= 1) {
-          ok = mbar_wait(bar(kBarOFull), (nb - 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after_sync();
-        }
-        tmem_st16x2(tmem + lane_off + kTmemP, pk);
-        const bool rescale_o = !wb.first() && alpha != 1.f;
-        if (__any_sync(0xffffffffu, rescale_o)) {
+        tc_fence_after_sync();
+      }
+      tmem_st16x2(tmem + lane_off + kTmemP, pk);
+      const bool rescale_o = !w.first() && alpha != 1.f;
+      if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            uint32_t o[16];
-            const uint32_t t_o = tmem + lane_off + kTmemO + 32u * c;
-            tmem_ld16x2(t_o, o);
-            tmem_wait_ld16(o);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[16];
+          const uint32_t t_o = tmem + lane_off + kTmemO + 32u * c;
+          tmem_ld16x2(t_o, o);
+          tmem_wait_ld16(o);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st16x2(t_o, o);
-          }
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16x2(t_o, o);
         }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (want_lo) atomicMax(const_cast<int*>(lo_flag) + (n & 1), n + 1);
+        mbar_arrive(bar(kBarPFull));
+      }
+      ++groups;
+
+      // ======== low part of P, when any warp of the CTA asked for it: every
+      // warp stores its own (zero where it did not ask) once the bf16 part's
+      // PV has read the buffer, and the PV warp adds P_lo V to O.
+      ok = mbar_wait(bar(kBarPFull), (groups - 1) & 1, abort_flag);  // every warp's request is in
+      if (!ok) break;
+      if (lo_flag[n & 1] == n + 1) {
+        ok = mbar_wait(bar(kBarOFull), (groups - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        tmem_st16x2(tmem + lane_off + kTmemP, lo);
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPFull));
+        ++groups;
+      }
 
-        // ---- epilogue at the end of a segment
-        if (wb.last()) {
-          const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
-          ok = mbar_wait(bar(kBarOFull), nb & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after_sync();
-          const int nsplit = __ldg(P.num_splits + wb.i + 1) - __ldg(P.num_splits + wb.i);
-          const bool direct = (nsplit == 1);
-          const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-          const float lse = (l_tot > 0.f) ? (m_run * c_log2 + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
-          const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + wb.i)) + wb.k;
+      // ======== epilogue at the end of a segment
+      if (w.last()) {
+        const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+        ok = mbar_wait(bar(kBarOFull), (groups - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int nsplit = __ldg(P.num_splits + w.i + 1) - __ldg(P.num_splits + w.i);
+        const bool direct = (nsplit == 1);
+        const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+        const float lse = (l_tot > 0.f) ? (m_run * c_log2 + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+        const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + w.i)) + w.k;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            // columns [64c, 64c+64) of this CTA's half: lane l takes 32 of them
-            uint32_t o[32];
-            tmem_ld16x2_32(tmem + lane_off + kTmemO + 64u * c, o);
-            tmem_wait_ld(o);
-            if (row_live) {
-              const int col = 256 * static_cast<int>(rank) + 64 * c + 32 * (lane_i >> 4);
-              // single-split sequences go straight to out, the pieces of the
-              // others to the workspace (bf16, normalised by their own sums)
-              __nv_bfloat16* const dst_row =
-                  direct ? static_cast<__nv_bfloat16*>(P.out) +
-                               ((static_cast<int64_t>(wb.i) * rows_total + row_in_seq) * kDimV + col)
-                         : static_cast<__nv_bfloat16*>(P.ws_o) + ((oslot * rows_total + row_in_seq) * kDimV + col);
-              uint4* dstp = reinterpret_cast<uint4*>(dst_row);
+        for (int c = 0; c < 4; ++c) {
+          // columns [64c, 64c+64) of this CTA's half: lane l takes 32 of them
+          uint32_t o[32];
+          tmem_ld16x2_32(tmem + lane_off + kTmemO + 64u * c, o);
+          tmem_wait_ld(o);
+          if (row_live) {
+            const int col = 256 * static_cast<int>(rank) + 64 * c + 32 * (lane_i >> 4);
+            if (direct) {
+              // single-split sequences go straight to out (bf16)
+              uint4* dstp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.out) +
+                                                     ((static_cast<int64_t>(w.i) * rows_total + row_in_seq) * kDimV + col));
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 uint4 v;
@@ -683,25 +741,28 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
                 v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
                 dstp[q] = v;
               }
+            } else {
+              // the pieces of the others go to the workspace, fp32, each
+              // normalised by its own sum
+              float4* dstp = reinterpret_cast<float4*>(static_cast<float*>(P.ws_o) +
+                                                       ((oslot * rows_total + row_in_seq) * kDimV + col));
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dstp[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                      __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
             }
           }
-          if (row_live && rank == 0 && lane_i < 16) {
-            if (direct)
-              P.lse[(static_cast<int64_t>(wb.i) * P.h_q + h) * P.s_q + j] = lse;
-            else
-              P.ws_lse[oslot * rows_total + row_in_seq] = lse;
-          }
-          tc_fence_before_sync();
         }
+        if (row_live && rank == 0 && lane_i < 16) {
+          if (direct)
+            P.lse[(static_cast<int64_t>(w.i) * P.h_q + h) * P.s_q + j] = lse;
+          else
+            P.ws_lse[oslot * rows_total + row_in_seq] = lse;
+        }
+        tc_fence_before_sync();
       }
-
-      // shift the skew: page n becomes the page to finish
-#pragma unroll
-      for (int c = 0; c < 32; ++c) a_prev[c] = a_cur[c];
-      wb = wa;
-      lim_b = lim_a;
-      if (wa.valid) wa.advance();
       ++n;
+      w.advance();
     }
     if (!ok) raise_status(P.status, kStatusTimeout);
   } else {

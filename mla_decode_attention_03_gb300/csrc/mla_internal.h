@@ -32,7 +32,7 @@ struct DecodeParams {
   const int32_t* num_splits;     // [b + 1] prefix sums
   void* out;                     // bf16 [b, s_q, h_q, 512]
   float* lse;                    // [b, h_q, s_q]
-  void* ws_o;                    // bf16 [slots, s_q*h_q, 512]: normalised partial outputs
+  void* ws_o;                    // fp32 [slots, s_q*h_q, 512]: normalised partial outputs
   float* ws_lse;                 // [slots, s_q*h_q]
   int32_t* status;
   int64_t num_blocks;
@@ -47,7 +47,7 @@ struct DecodeParams {
 
 struct CombineParams {
   const int32_t* num_splits;
-  const void* ws_o;              // bf16 partial outputs
+  const void* ws_o;              // fp32 partial outputs
   const float* ws_lse;
   void* out;
   float* lse;

@@ -203,19 +203,15 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams P)
     for (int k = 0; k < ns; ++k) {
       const int64_t r = static_cast<int64_t>(s0 + k) * rows + row;
       const float wgt = expf(P.ws_lse[r] - lse);
-      // lane l merges columns [16l, 16l+16): two 16-byte loads of bf16 pairs
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.ws_o) + r * kDimV) +
-                         lane * 2;
+      // lane l merges columns [16l, 16l+16): four 16-byte loads of fp32
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r * kDimV) + lane * 4;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint4 v = src[q];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-          acc[8 * q + 2 * e] += wgt * f.x;
-          acc[8 * q + 2 * e + 1] += wgt * f.y;
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q];
+        acc[4 * q + 0] += wgt * v.x;
+        acc[4 * q + 1] += wgt * v.y;
+        acc[4 * q + 2] += wgt * v.z;
+        acc[4 * q + 3] += wgt * v.w;
       }
     }
   }

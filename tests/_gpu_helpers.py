@@ -6,15 +6,8 @@ import torch
 import oracle
 from mla_decode_attention_03_gb300 import ops
 
-# Tolerance: |d out| <= ATOL + RTOL * scale and |d lse| <= LSE_TOL.  The
-# relative term is read against the magnitude of the output row (one (i, j, h)
-# vector, a single softmax-weighted average of V rows): scale = max |out_oracle|
-# over that row.  The stricter elementwise form (scale = |out_oracle| of the
-# element itself) is also asserted on every workload except those with
-# deliberately peaky keys: there the weights are rounded to bf16 -- the operand
-# type the tensor cores require next to a bf16 cache -- with a relative error
-# up to 2^-8 each, and x4-scaled value rows that cancel can push single
-# near-zero elements past 1e-2 absolute while the row stays within 0.2%.
+# Tolerance, element by element: |d out| <= ATOL + RTOL * |out_oracle| and
+# |d lse| <= LSE_TOL, on every workload.
 ATOL, RTOL, LSE_TOL = 1e-2, 2e-2, 1e-3
 
 
@@ -43,34 +36,33 @@ def oracle_rows(w, rows):
                               dv=w.dv, softmax_scale=w.softmax_scale, causal=w.causal)
 
 
-def compare_rows(w, out, lse, rows):
+def compare_rows(w, out, lse, rows, chunk=8192):
     """out [b, s_q, h_q, 512] bf16 and lse [b, h_q, s_q] from the GPU vs the
-    oracle at `rows` (n x 3 of i, j, h).  Returns (max_out_excess, max_lse_err)."""
+    oracle at `rows` (n x 3 of i, j, h), in chunks of rows.  Returns
+    (max elementwise excess over the tolerance, max |d lse|)."""
     rows = np.asarray(rows, dtype=np.int32).reshape(-1, 3)
-    o_ref, l_ref = oracle_rows(w, rows)
-    o = out.float().cpu().numpy().astype(np.float64)
+    o = out.float().cpu().numpy()
     l = lse.float().cpu().numpy().astype(np.float64)
-    i, j, h = rows[:, 0], rows[:, 1], rows[:, 2]
-    o_gpu = o[i, j, h]
-    l_gpu = l[i, h, j]
-    assert np.all(np.isfinite(o_gpu)), "non-finite output"
-    err = np.abs(o_gpu - o_ref)
-    row_scale = np.abs(o_ref).max(axis=1, keepdims=True)
-    excess_row = err - (ATOL + RTOL * row_scale)
-    excess_elem = err - (ATOL + RTOL * np.abs(o_ref))
-    fin = np.isfinite(l_ref)
-    assert np.array_equal(np.isfinite(l_gpu), fin), "lse -inf pattern differs"
-    assert np.all(l_gpu[~fin] == l_ref[~fin])
-    lerr = np.abs(l_gpu[fin] - l_ref[fin])
-    return (float(excess_row.max(initial=-1.0)), float(excess_elem.max(initial=-1.0)),
-            float(lerr.max(initial=0.0)))
+    ex_elem, lerr = -1.0, 0.0
+    for c0 in range(0, len(rows), chunk):
+        r = rows[c0:c0 + chunk]
+        o_ref, l_ref = oracle_rows(w, r)
+        i, j, h = r[:, 0], r[:, 1], r[:, 2]
+        o_gpu = o[i, j, h].astype(np.float64)
+        l_gpu = l[i, h, j]
+        assert np.all(np.isfinite(o_gpu)), "non-finite output"
+        err = np.abs(o_gpu - o_ref) - (ATOL + RTOL * np.abs(o_ref))
+        ex_elem = max(ex_elem, float(err.max(initial=-1.0)))
+        fin = np.isfinite(l_ref)
+        assert np.array_equal(np.isfinite(l_gpu), fin), "lse -inf pattern differs"
+        assert np.all(l_gpu[~fin] == l_ref[~fin])
+        lerr = max(lerr, float(np.abs(l_gpu[fin] - l_ref[fin]).max(initial=0.0)))
+    return ex_elem, lerr
 
 
 def assert_matches(w, out, lse, rows):
-    ex_row, ex_elem, le = compare_rows(w, out, lse, rows)
-    assert ex_row <= 0.0, f"out outside |d| <= {ATOL} + {RTOL}*rowmax|ref| by {ex_row:.3e}"
-    if "peaky_slots" not in w.extra:
-        assert ex_elem <= 0.0, f"out outside |d| <= {ATOL} + {RTOL}|ref| by {ex_elem:.3e}"
+    ex_elem, le = compare_rows(w, out, lse, rows)
+    assert ex_elem <= 0.0, f"out outside |d| <= {ATOL} + {RTOL}|ref| by {ex_elem:.3e}"
     assert le <= LSE_TOL, f"lse error {le:.3e} > {LSE_TOL}"
 
 

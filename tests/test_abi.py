@@ -88,8 +88,8 @@ def test_sizes_and_strings(lib):
     lib.mla_metadata_ints.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_status_string.argtypes = [ctypes.c_int32]
-    # (b + parts) slots x rows x 512 bf16, then (b + parts) x rows fp32 lse, each 256-byte aligned
-    o = (128 + 76) * 128 * 512 * 2
+    # (b + parts) slots x rows x 512 fp32, then (b + parts) x rows fp32 lse, each 256-byte aligned
+    o = (128 + 76) * 128 * 512 * 4
     l = (128 + 76) * 128 * 4
     assert lib.mla_workspace_bytes(128, 1, 128, 76) == o + ((l + 255) // 256) * 256
     assert lib.mla_workspace_bytes(0, 1, 128, 76) == 0

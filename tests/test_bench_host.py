@@ -36,5 +36,6 @@ def test_kernel_digest_ignores_comments_not_code(tmp_path, monkeypatch):
     text = f.read_text(encoding="utf-8")
     f.write_text("// an added comment line\n" + text.replace("\n", "\n  ", 3), encoding="utf-8")
     assert bench.kernel_digest() == base  # comments and whitespace only
-    f.write_text(text.replace("kStages = 4", "kStages = 3", 1), encoding="utf-8")
+    assert "kStages = 5" in text
+    f.write_text(text.replace("kStages = 5", "kStages = 4", 1), encoding="utf-8")
     assert bench.kernel_digest() != base  # a code change

@@ -60,7 +60,7 @@ def test_header_compiles_as_c99_and_links(tmp_path, lib_path):
     out = dict(line.split(" ", 1) for line in r.stdout.strip().splitlines())
     # costs 65, 65, 1, 2, 3, 65 (pages + 1): total 201, targets 67 and 134
     assert out["chunks"] == "3: 0 2 5 6"
-    o = (128 + 76) * 128 * 512 * 2
+    o = (128 + 76) * 128 * 512 * 4  # fp32 partial outputs
     lse = (128 + 76) * 128 * 4
     assert int(out["workspace"]) == o + (lse + 255) // 256 * 256
     assert int(out["metadata"]) == 76 * 8

@@ -7,10 +7,12 @@ vLLM runs note enforce_eager, i.e. the graph-captured path is the serving
 default.  The C ABI allocates nothing and never synchronises, so the step
 (metadata + three layers of decode and combine) can be captured once and
 replayed; replays must equal the eager calls, also after the inputs change in
-place.
+place, and the first replay is checked against the fp64 oracle on every row.
 """
 import pytest
 import torch
+
+from tests._gpu_helpers import all_rows, assert_matches
 
 from mla_decode_attention_03_gb300 import ops
 from mla_decode_attention_03_gb300 import workloads as W
@@ -21,12 +23,14 @@ LAYERS = 3
 
 
 def _layer_inputs(seed, stride=640):
-    # same lengths and block table for every layer (one step), different q and cache
-    return W.make(6, 1, 128, 1, [700, 64, 3000, 1, 129, 4096], stride=stride, seed=seed)
+    # same lengths and block table for every layer (one step: pages in order,
+    # so every layer's table is the same), different q and cache
+    return W.make(6, 1, 128, 1, [700, 64, 3000, 1, 129, 4096], stride=stride, seed=seed, permute=False)
 
 
 def test_captured_step_equals_eager_and_tracks_new_inputs():
     ws = [_layer_inputs(40 + k) for k in range(LAYERS)]
+    assert all(torch.equal(w.block_table, ws[0].block_table) for w in ws)
     sl = ws[0].cache_seqlens.cuda()
     bt = ws[0].block_table.cuda()
     qs = [w.q.cuda() for w in ws]
@@ -61,6 +65,8 @@ def test_captured_step_equals_eager_and_tracks_new_inputs():
     ops.check_status(dec.status)
     for (o, l), (ro, rl) in zip(zip(outs, lses), ref):
         assert torch.equal(o, ro) and torch.equal(l, rl)
+    for w, o, l in zip(ws, outs, lses):
+        assert_matches(w, o, l, all_rows(w))
 
     # new q values in place: the replay must follow them
     for k in range(LAYERS):

@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
-Small shapes are compared element by element on every output row; the five
-named workloads at their full sizes are compared on sampled rows, in the
-launch configuration the benchmark times (the recommended number of parts).
+Every test compares every output row element by element: small shapes that
+span several pages, ragged tails and the degenerate cases, and the five named
+workloads at their full sizes in the launch configuration the benchmark times
+(the recommended number of parts).
 Tolerance: |d out| <= 1e-2 + 2e-2 |out_oracle| and |d lse| <= 1e-3.
 """
 import zlib
@@ -13,7 +14,7 @@ import torch
 
 from mla_decode_attention_03_gb300 import ops
 from mla_decode_attention_03_gb300 import workloads as W
-from tests._gpu_helpers import all_rows, assert_matches, run_gpu, sample_rows, to_device
+from tests._gpu_helpers import all_rows, assert_matches, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -50,18 +51,54 @@ def test_named_small_all_rows(name):
 
 
 @pytest.mark.parametrize("name,stride", [("bench", 576), ("bench", 640), ("mtp", None), ("skewed", None)])
-def test_named_full_size_sampled(name, stride):
+def test_named_full_size_all_rows(name, stride):
     w = W.named(name, stride=stride)
     out, lse, _, nsplit = run_gpu(w)
-    last = [w.b - 1, w.s_q - 1, w.h_q - 1]
-    extra = [[0, 0, 0], last]
-    if name == "skewed":  # the two long sequences, every 16th head
-        extra += [[i, 0, h] for i in (0, 1) for h in range(0, w.h_q, 16)]
-    rows = sample_rows(w, 384, seed=1, extra=extra)
+    assert_matches(w, out, lse, all_rows(w))
+
+
+def test_lazy_rescale_every_page():
+    """The running max is moved (and O and the row sums rescaled) only when it
+    grows by more than 8 log2 units.  Here one key per page climbs by about 9.6
+    log2 units over the previous page's (q has 4 in dim 0 for every head, the
+    climbing key 40*(p+1) there), so the rescale runs on nearly every page of
+    every row, while the other keys of earlier pages still carry weight that a
+    wrong rescale factor would distort by 2^9.  Sequences are cut into several
+    pieces so the merge of rescaled pieces is covered too."""
+    lens = [6 * 64, 5 * 64 - 17, 7 * 64 + 3, 64]
+    w = W.make(len(lens), 1, 128, 1, lens, stride=640, seed=27)
+    w.q[..., 0] = 4.0
+    bt = w.block_table.numpy()
+    for i, L in enumerate(lens):
+        for p in range(-(-L // 64)):
+            tok = (5 + 7 * p) % min(64, L - 64 * p)  # a visible slot of page p
+            w.kcache_alloc[int(bt[i, p]), tok, 0, 0] = 40.0 * (p + 1)
+    for parts in (None, 9):
+        out, lse, _, _ = run_gpu(w, parts=parts)
+        assert_matches(w, out, lse, all_rows(w))
+
+
+def test_negative_length_reported_and_treated_as_empty():
+    """A negative cache_seqlens entry is outside the contract; the scheduler
+    reports MLA_ERR_BAD_SEQLEN in the status word, the decode treats that
+    sequence as empty (no page of it is read), and the context stays usable."""
+    w = W.make(3, 1, 128, 1, [200, 64, 300], seed=26)
+    dev = to_device(w)
+    sl = dev["cache_seqlens"].clone()
+    sl[1] = -5
+    status = ops.new_status()
+    meta, nsplit = ops.get_mla_metadata(sl, 4, status)
+    out, lse = ops.mla_decode_with_kvcache(dev["q"], dev["kcache"], dev["block_table"], sl, meta, nsplit,
+                                           w.softmax_scale, False, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -7
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    rows = all_rows(w)
+    rows = rows[rows[:, 0] != 1]
     assert_matches(w, out, lse, rows)
-    # every output row must have been written (no NaN, no untouched garbage)
-    assert torch.isfinite(out.float()).all()
-    assert torch.isfinite(lse).all()
+    w_ok = W.make(1, 1, 16, 1, [64], seed=25)
+    out, lse, _, _ = run_gpu(w_ok)
+    assert_matches(w_ok, out, lse, all_rows(w_ok))
 
 
 def test_stride_576_and_640_identical():
