@@ -39,7 +39,8 @@ import torch  # noqa: E402
 from mla_decode_attention_03_gb300 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
-BREAKDOWN_EVERY = 8  # every 8th timed step also times each kernel on its own
+BREAKDOWN_EVERY = 8  # every 8th timed pass also times each kernel on its own
+MIN_TIMED_S = 1.0    # the timed loop lasts at least this long, so that clock samples fall inside it
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch,
 # taken from one ncu capture, keyed by a digest of the kernel's sources (comments
@@ -52,12 +53,19 @@ MEASURED_TRAFFIC = {
 
 
 def breakdown_steps(steps: int):
-    """Indices of the timed steps that also carry events between the kernels
-    (every BREAKDOWN_EVERY-th, at least one) and of the plain steps `value`
-    is taken from (all steps if there are no others)."""
+    """Indices of the timed passes that also carry events between the kernels
+    (every BREAKDOWN_EVERY-th, at least one) and of the plain passes `value`
+    is taken from (all passes if there are no others)."""
     inner = [k for k in range(steps) if k % BREAKDOWN_EVERY == BREAKDOWN_EVERY - 1] or [steps - 1]
     plain = [k for k in range(steps) if k not in set(inner)] or list(range(steps))
     return inner, plain
+
+
+def passes_per_step(steps: int, seconds_per_pass: float, min_seconds: float = MIN_TIMED_S) -> int:
+    """Passes of the hot path per timed step, so that `steps` steps last at
+    least `min_seconds` (one pass per step when they already do)."""
+    need = min_seconds / max(steps * seconds_per_pass, 1e-9)
+    return max(1, int(np.ceil(need)))
 
 
 def kernel_digest() -> str:
@@ -207,12 +215,14 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    # Every timed step is bracketed by two events (ev[0], ev[3]); the three
-    # kernels then run back to back, each starting its set-up while the one
-    # before it finishes (programmatic dependent launch).  Every
-    # BREAKDOWN_EVERY-th step also records events between the kernels (which
-    # serialises them) for the per-kernel breakdown and the decode kernel's own
-    # duration; `value` comes from the other steps.
+    # A timed step is R passes of the hot path over the batch, R chosen so the
+    # K timed steps last at least MIN_TIMED_S (clock samples then fall inside
+    # the loop).  Every pass is bracketed by two events (ev[0], ev[3]) with the
+    # L2 flush outside them; the three kernels run back to back, each starting
+    # its set-up while the one before it finishes (programmatic dependent
+    # launch).  Every BREAKDOWN_EVERY-th pass also records events between the
+    # kernels (which serialises them) for the per-kernel breakdown and the
+    # decode kernel's own duration; `value` comes from the other passes.
     def step(ev=None, inner=False):
         if ev is not None:
             ev[0].record(stream)
@@ -227,8 +237,6 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[3].record(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    inner_steps, plain = breakdown_steps(args.steps)
     # the clock sampler starts before the warm-up so that its own start-up falls
     # outside the timed loop; only samples taken during the loop are kept
     with ClockSampler(local) as clk:
@@ -237,12 +245,23 @@ def run_ours(args, world, rank, local):
             step()
         torch.cuda.synchronize()
         ops.check_status(dec.status)
+        # wall time of one pass with its flush, for the passes per step
+        tp0 = time.perf_counter()
+        for k in range(5):
+            flush.fill_(k)
+            step()
+        torch.cuda.synchronize()
+        reps = passes_per_step(args.steps, (time.perf_counter() - tp0) / 5)
+        reps = int(max_over_ranks(float(reps), world))
+        total = args.steps * reps
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(total)]
+        inner_passes, plain = breakdown_steps(total)
+        inner_set = set(inner_passes)
         barrier(world)
         torch.cuda.synchronize()
-        inner_set = set(inner_steps)
         t0 = time.perf_counter()
-        for k in range(args.steps):
-            flush.fill_(k & 0xFF)  # L2 flush: a 512 MB write between steps, outside the events
+        for k in range(total):
+            flush.fill_(k & 0xFF)  # L2 flush: a 512 MB write between passes, outside the events
             step(evs[k], inner=(k in inner_set))
         torch.cuda.synchronize()
         t1 = time.perf_counter()
@@ -250,11 +269,12 @@ def run_ours(args, world, rank, local):
     clk.window(t0, t1)
     barrier(world)
     ops.check_status(dec.status)
-    t_meta = [evs[k][0].elapsed_time(evs[k][1]) for k in inner_steps]
-    t_dec = [evs[k][1].elapsed_time(evs[k][2]) for k in inner_steps]
-    t_comb = [evs[k][2].elapsed_time(evs[k][3]) for k in inner_steps]
-    t_step = [evs[k][0].elapsed_time(evs[k][3]) for k in plain]
-    ms_step = max_over_ranks(float(np.mean(t_step)), world)
+    t_meta = [evs[k][0].elapsed_time(evs[k][1]) for k in inner_passes]
+    t_dec = [evs[k][1].elapsed_time(evs[k][2]) for k in inner_passes]
+    t_comb = [evs[k][2].elapsed_time(evs[k][3]) for k in inner_passes]
+    t_pass = [evs[k][0].elapsed_time(evs[k][3]) for k in plain]
+    ms_pass = max_over_ranks(float(np.mean(t_pass)), world)
+    ms_step = ms_pass * reps
     ms_dec = float(np.mean(t_dec))
 
     # end to end through the public API: pinned host q / block_table / seqlens in,
@@ -269,7 +289,8 @@ def run_ours(args, world, rank, local):
 
     hbm_peak, tf_peak, peak_src = peaks()
     achieved = nbytes / 1e9 / (ms_dec / 1e3)
-    value = world * nbytes / 1e6 / ms_step
+    value = world * nbytes / 1e6 / ms_pass
+    clocks = clk.summary()
     line = {
         "metric": "MLA decode achieved GB/s (pages' bandwidth formula), whole step",
         "value": round(value, 1),
@@ -289,14 +310,16 @@ def run_ours(args, world, rank, local):
             "sum_seqlens": int(w.cache_seqlens.sum()),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "num_parts": parts,
-            "l2": "flushed between steps by a 512 MB write outside the timed events",
-            "step": "metadata + split-KV decode + combine",
-            "timing": f"value from the {len(plain)} steps timed with two events each; "
-                      f"breakdown and roofline from the {len(inner_steps)} steps (every {BREAKDOWN_EVERY}th) "
-                      "with events between the kernels",
-            "bytes_per_step": nbytes, "flops_per_step": flops,
+            "l2": "flushed between passes by a 512 MB write outside the timed events",
+            "step": f"{reps} pass(es) of metadata + split-KV decode + combine over the batch",
+            "passes_per_step": reps,
+            "timing": f"{args.steps} steps x {reps} passes = {total} passes in {wall:.2f} s; value from the "
+                      f"{len(plain)} passes timed with two events each; breakdown and roofline from the "
+                      f"{len(inner_passes)} passes (every {BREAKDOWN_EVERY}th) with events between the kernels",
+            "bytes_per_pass": nbytes, "flops_per_pass": flops,
         },
-        "tflops": round(world * flops / 1e9 / ms_step, 1),
+        "ms_per_pass": round(ms_pass, 5),
+        "tflops": round(world * flops / 1e9 / ms_pass, 1),
         "breakdown_us": {"metadata": round(1e3 * float(np.mean(t_meta)), 2),
                          "decode": round(1e3 * ms_dec, 2),
                          "combine": round(1e3 * float(np.mean(t_comb)), 2),
@@ -310,9 +333,13 @@ def run_ours(args, world, rank, local):
                      "tensor_frac": round(flops / 1e9 / ms_dec / tf_peak, 4)},
         "e2e": e2e,
         **({"e2e_runs": e2e_runs} if e2e_runs else {}),
-        "gpu_launches": 3 * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": 3 * total,
+        "clocks": clocks,
     }
+    if clocks.get("sm_mhz"):
+        # the pass time in SM cycles at the median clock under load
+        line["clock_normalised"] = {"sm_cycles_per_pass": round(ms_pass * 1e-3 * clocks["sm_mhz"] * 1e6),
+                                    "decode_sm_cycles": round(ms_dec * 1e-3 * clocks["sm_mhz"] * 1e6)}
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -356,10 +383,39 @@ def run_e2e(args, w, dev, kc, parts, dec, flush, nbytes, chunks=0):
     ops.check_status(hd.status)
     hd.close()
     ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+    link = host_link(dev, h2d, d2h, stream)
+    link["copies_fraction_of_step"] = round(link["copies_ms"] / ms, 3)
     return {"value": round(nbytes / 1e6 / ms, 1), "unit": "GB/s", "ms_per_step": round(ms, 5), "runs": runs,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "host_link": link,
             "note": f"mla_decode_host: pinned host q/block_table/seqlens in, out/lse out, {runs} run(s) of "
                     "sequences with copies overlapping the decode; the KV cache stays resident"}
+
+
+def host_link(dev, h2d: int, d2h: int, stream, reps: int = 20) -> dict:
+    """The host link's own rate for the step's copy sizes: one plain
+    cudaMemcpyAsync of h2d bytes from pinned host memory to the device, and one
+    of d2h bytes back, each timed alone with CUDA events (median of `reps`)."""
+    def timed(dst, src):
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in ts]))
+    h_in = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(d2h, dtype=torch.uint8, device=dev)
+    h_out = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+    ms_in = timed(d_in, h_in)
+    ms_out = timed(h_out, d_out)
+    return {"h2d_gbs": round(h2d / 1e6 / ms_in, 1), "d2h_gbs": round(d2h / 1e6 / ms_out, 1),
+            "copies_ms": round(ms_in + ms_out, 5),
+            "note": "plain pinned cudaMemcpyAsync of the step's copy sizes, each direction alone"}
 
 
 # ----------------------------------------------------------- CPU baseline

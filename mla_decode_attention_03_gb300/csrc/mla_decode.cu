@@ -37,12 +37,17 @@
 //    and the epilogue, each over 16 full rows (half a tensor-memory lane
 //    quadrant) and all 64 tokens of a page, so a row's max and sum need one
 //    warp shuffle and no other warp.
-//  * The softmax loop is skewed by one page: it reads its partial S(n) (which
-//    the sender warps quantise and send meanwhile), then finishes page n-1,
-//    whose peer partial arrived while it worked on page n.  QK runs two pages ahead of the
-//    softmax; an S buffer is handed back as soon as it has been read.  The
-//    tensor core executes MMAs in issue order, so QK(n) waits until PV(n-3) has
-//    been issued: PV never queues behind QKs that are not yet needed.
+//  * Page n flows in order: QK(n) -> the sender warps quantise and send the
+//    partial while the softmax warps read theirs -> the peer's partial lands ->
+//    softmax -> P -> PV(n).  QK runs up to two pages ahead of the softmax (two
+//    S buffers, each handed back as soon as the softmax has read it); five K
+//    stages keep the HBM latency (about 1.3 us under load) covered.  Holding
+//    QK back until PV(n-3) had been issued, or prefetching S a page early, was
+//    measured slower and dropped.
+//  * P is rounded to bf16 for the tensor cores.  On pages where one weight
+//    exceeds a quarter of its row half's running sum, a second PV pass adds
+//    P_lo V (P_lo = the bf16 rounding error of P, itself in bf16), so cancelling
+//    value rows under a few dominant keys stay within the tolerance.
 //  * Exchange slots are returned to the sender by an explicit credit: each
 //    softmax warp that has read its part of a slot fences (CTA scope) and
 //    counts; the warp that completes the count of 8 sends one relaxed remote
@@ -99,15 +104,7 @@ constexpr int kBarPFull = kBarSFree + 2;
 constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
 constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: the peer has read the slot
-// PV of page n has been issued, one barrier per page mod 4.  QK(n) waits for
-// PV(n-3); PV(n+1) -- the next page on the same barrier -- cannot be issued
-// before QK(n) (its softmax needs S(n) first), so the barrier is never two
-// phases ahead of that wait.  With two barriers (page parity) PV(n-3) and
-// PV(n-1) could both be issued while QK(n) waited for its K page, and the
-// parity wait would then hang until PV(n+1).
-constexpr int kPVIssuedBars = 4;
-constexpr int kBarPVIssued = kBarXEmpty + kXSlots;
-constexpr int kBarDone = kBarPVIssued + kPVIssuedBars;
+constexpr int kBarDone = kBarXEmpty + kXSlots;
 constexpr int kNumBars = kBarDone + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -221,6 +218,40 @@ __device__ __forceinline__ uint32_t x_scale(int sw, int lane) {
   return static_cast<uint32_t>(kXData + (sw * 32 + lane) * 4);
 }
 
+// O <- alpha * O for this warp's 16 rows of the CTA's O half (columns
+// [0, 256) of tensor memory from `t_o`), in eight 32-column steps.
+__device__ __noinline__ void rescale_o_half(uint32_t t_o, float alpha) {
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    uint32_t o[16];
+    tmem_ld16x2(t_o + 32u * c, o);
+    tmem_wait_ld16(o);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+    tmem_st16x2(t_o + 32u * c, o);
+  }
+}
+
+// The low-part pass of page `page`, run by every softmax warp once all of them
+// have handed that page's bf16 P over (the PFull phase `groups - 1`): if any
+// warp asked for it (the flag holds page + 1), wait until the bf16 part's PV
+// has read the P buffer, store this warp's low part (zero where it did not
+// ask) and hand it over as one more PV group.  Returns false on abort.
+__device__ __forceinline__ bool lo_pass(uint32_t pfull, uint32_t ofull, volatile int* lo_flag, int page, int& groups,
+                                        uint32_t t_p, const uint32_t (&lo)[16], volatile int* abort_flag) {
+  if (!mbar_wait(pfull, (groups - 1) & 1, abort_flag)) return false;  // every warp's request is in
+  if (lo_flag[page & 1] != page + 1) return true;
+  if (!mbar_wait(ofull, (groups - 1) & 1, abort_flag)) return false;
+  tc_fence_after_sync();
+  tmem_st16x2(t_p, lo);
+  tmem_wait_st();
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane_id() == 0) mbar_arrive(pfull);
+  ++groups;
+  return mbar_wait(ofull, (groups - 1) & 1, abort_flag);  // the low part's PV is complete
+}
+
 // ----------------------------------------------------------------- kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_constant__ CUtensorMap k_lat,
@@ -263,7 +294,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarSFree + s), 8 + 4);  // softmax warps + sender warps
     }
     mbar_init(bar(kBarPFull), 8);
-    for (int s = 0; s < kPVIssuedBars; ++s) mbar_init(bar(kBarPVIssued + s), 1);
     mbar_init(bar(kBarOFull), 1);
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(bar(kBarXFull + s), 1);
@@ -371,9 +401,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     // ================================================= PV issuer
     // Warp 5 issues PV; QK is issued by warps 6 and 7 (even and odd pages).
     // Splitting the tcgen05.mma issue over three sub-partitions keeps any one of
-    // them from starving the two softmax warps it hosts.  The tensor core runs
-    // MMAs in issue order, so QK(n) is issued only after PV(n-3): a PV never
-    // queues behind QKs that are not needed yet.
+    // them from starving the two softmax warps it hosts (one thread issues at
+    // most one MMA per ~52 cycles, so the 18 N=64 MMAs of a page's QK take about
+    // 950 cycles to issue).
     if (lane == 0) {
       // V = this CTA's 256 latent dims of the page, read MN-major:
       // 64-dim column blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
@@ -400,7 +430,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         const bool lo = (lo_flag[np & 1] == np + 1);
         if (!lo) umma_commit(bar(kBarEmpty + st));
         umma_commit(bar(kBarOFull));
-        mbar_arrive(bar(kBarPVIssued + (np % kPVIssuedBars)));
         if (lo) {
           ok = mbar_wait(bar(kBarPFull), kp & 1, abort_flag);
           if (!ok) break;
@@ -449,10 +478,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         if ((n & 1) == parity) {
           if (n >= 2) {
             ok = mbar_wait(bar(kBarSFree + parity), ((n >> 1) - 1) & 1, abort_flag);
-            if (!ok) break;
-          }
-          if (n >= 3) {
-            ok = mbar_wait(bar(kBarPVIssued + ((n - 3) % kPVIssuedBars)), ((n - 3) / kPVIssuedBars) & 1, abort_flag);
             if (!ok) break;
           }
           const int st = n % kStages;
@@ -536,6 +561,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     int lim = 0;
     int n = 0;
     int groups = 0;  // P hand-offs to the PV warp so far (two on pages with a low-part pass)
+    int lo_check = -1;  // page whose low-part decision is still open, or -1
+    uint32_t lo[16];    // that page's low part of P (zero if this warp did not ask)
     bool ok = true;
     while (ok && w.valid) {
       if (w.first()) {
@@ -585,6 +612,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           }
         }
       }
+
       // The slot has been read: the last of the 8 softmax warps to finish
       // returns it to the peer's senders.  Each warp's fence orders its lanes'
       // loads (after the warp barrier) before its count; the last warp's fence
@@ -630,10 +658,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       // Does a weight of this warp's lanes exceed a quarter of its running sum?
       // (-inf lanes give 0, NaN compares false.)
       const bool want_lo = __any_sync(0xffffffffu, ex2_approx(fmaf(mx_lane, c_log2, neg_mc)) * kLoRatio > l_run * alpha);
-      uint32_t pk[16], lo[16];
+      uint32_t pk[16];
       float rsum;
       {
-        const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc), neg1 = f2(-1.f, -1.f);
+        const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
         uint64_t sum2[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) sum2[u] = f2(0.f, 0.f);
@@ -645,16 +673,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           const float e1 = ex2_approx(a1);
           sum2[c & 3] = f2_add(sum2[c & 3], f2(e0, e1));
           pk[c] = pack_bf16x2(e0, e1);
-          if (want_lo) {
-            // the bf16 rounding error of the pair, itself rounded to bf16
-            float r0, r1;
-            f2_split(f2_fma(f2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)), neg1,
-                            f2(e0, e1)),
-                     r0, r1);
-            lo[c] = pack_bf16x2(r0, r1);
-          } else {
-            lo[c] = 0u;
-          }
         }
         float sum8[8];
 #pragma unroll
@@ -662,27 +680,24 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       }
       l_run = l_run * alpha + rsum;  // this lane's 32 tokens; the row sum adds lane l^16's
-      // Every PV issued so far must be complete: it read the P buffer, and O
-      // is rescaled below.
+
+      // The previous page's low part, if any warp asked for it: once its bf16
+      // part's PV is complete (it read the P buffer), every warp stores its own
+      // low part (zero where it did not ask) and the PV warp adds P_lo V to O.
       if (groups > 0) {
         ok = mbar_wait(bar(kBarOFull), (groups - 1) & 1, abort_flag);
         if (!ok) break;
+        if (lo_check >= 0) {
+          ok = lo_pass(bar(kBarPFull), bar(kBarOFull), lo_flag, lo_check, groups, tmem + lane_off + kTmemP, lo,
+                       abort_flag);
+          if (!ok) break;
+          lo_check = -1;
+        }
         tc_fence_after_sync();
       }
       tmem_st16x2(tmem + lane_off + kTmemP, pk);
       const bool rescale_o = !w.first() && alpha != 1.f;
-      if (__any_sync(0xffffffffu, rescale_o)) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t o[16];
-          const uint32_t t_o = tmem + lane_off + kTmemO + 32u * c;
-          tmem_ld16x2(t_o, o);
-          tmem_wait_ld16(o);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st16x2(t_o, o);
-        }
-      }
+      if (__any_sync(0xffffffffu, rescale_o)) rescale_o_half(tmem + lane_off + kTmemO, alpha);
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
@@ -691,22 +706,30 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         mbar_arrive(bar(kBarPFull));
       }
       ++groups;
-
-      // ======== low part of P, when any warp of the CTA asked for it: every
-      // warp stores its own (zero where it did not ask) once the bf16 part's
-      // PV has read the buffer, and the PV warp adds P_lo V to O.
-      ok = mbar_wait(bar(kBarPFull), (groups - 1) & 1, abort_flag);  // every warp's request is in
-      if (!ok) break;
-      if (lo_flag[n & 1] == n + 1) {
-        ok = mbar_wait(bar(kBarOFull), (groups - 1) & 1, abort_flag);
+      // This page's low part is decided once every warp has handed P over:
+      // before the next P store, or right here at the end of a segment.
+      if (want_lo) {
+        const uint64_t c2 = f2(c_log2, c_log2), nmc2 = f2(neg_mc, neg_mc);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          // the bf16 rounding error of the pair (same weights as above), itself rounded to bf16
+          float a0, a1, r0, r1;
+          f2_split(f2_fma(f2(x[2 * c], x[2 * c + 1]), c2, nmc2), a0, a1);
+          f2_split(f2_sub(f2(ex2_approx(a0), ex2_approx(a1)),
+                          f2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u))),
+                   r0, r1);
+          lo[c] = pack_bf16x2(r0, r1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) lo[c] = 0u;
+      }
+      lo_check = n;
+      if (w.last()) {
+        ok = lo_pass(bar(kBarPFull), bar(kBarOFull), lo_flag, lo_check, groups, tmem + lane_off + kTmemP, lo,
+                     abort_flag);
         if (!ok) break;
-        tc_fence_after_sync();
-        tmem_st16x2(tmem + lane_off + kTmemP, lo);
-        tmem_wait_st();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull));
-        ++groups;
+        lo_check = -1;
       }
 
       // ======== epilogue at the end of a segment

@@ -39,3 +39,12 @@ def test_kernel_digest_ignores_comments_not_code(tmp_path, monkeypatch):
     assert "kStages = 5" in text
     f.write_text(text.replace("kStages = 5", "kStages = 4", 1), encoding="utf-8")
     assert bench.kernel_digest() != base  # a code change
+
+
+def test_passes_per_step_make_the_timed_loop_last():
+    # 20 steps of 0.18 ms need 278 passes each to reach one second
+    assert bench.passes_per_step(20, 0.18e-3, 1.0) == 278
+    assert 20 * 278 * 0.18e-3 >= 1.0 > 20 * 277 * 0.18e-3
+    # steps that already last long enough run one pass each
+    assert bench.passes_per_step(20000, 0.18e-3, 1.0) == 1
+    assert bench.passes_per_step(1, 5.0, 1.0) == 1
