@@ -173,6 +173,27 @@ mla_status_t mla_combine_splits(const int32_t *num_splits, int b, int s_q, int h
                                 mla_stream_t stream);
 
 /*
+ * Diagnostic of the decode kernel's failure detection (no counterpart on the
+ * pages).  Same arguments and host-side checks as mla_decode_with_kvcache, but
+ * the kernel's TMA producer first waits on a barrier that nothing ever
+ * completes, before it issues any copy.  Every wait in the kernel is bounded
+ * (about 2 s): that wait gives up, raises the CTA's abort flag, every other
+ * warp role leaves its own wait, the CTAs free their tensor memory and exit,
+ * and MLA_ERR_TIMEOUT (-6) is written to *status.  out and lse are left
+ * undefined.  The device stays usable: the next call decodes normally.  Lets a
+ * caller check that a wait that can never end is reported, not hung on.
+ */
+mla_status_t mla_selftest_wait_timeout(const void *q, int b, int s_q, int h_q, int d,
+                                       const void *kcache, int64_t num_blocks, int block_size,
+                                       int h_kv, int stride, const int32_t *block_table,
+                                       int max_blocks_per_seq, const int32_t *cache_seqlens,
+                                       int dv, const int32_t *metadata, int num_parts,
+                                       const int32_t *num_splits, float softmax_scale,
+                                       int causal, void *out, float *lse, void *workspace,
+                                       size_t workspace_bytes, int32_t *status,
+                                       mla_stream_t stream);
+
+/*
  * Cache maintenance next to the decode (MLA caches have one latent KV head).
  *
  * mla_write_cache puts new tokens into the paged cache the decode reads:

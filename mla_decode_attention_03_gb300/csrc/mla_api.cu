@@ -171,7 +171,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
                          const int32_t* cache_seqlens, int dv, const int32_t* metadata, int num_parts,
                          const int32_t* num_splits, float softmax_scale, int causal, void* out,
                          float* lse, void* workspace, size_t workspace_bytes, int32_t* status,
-                         mla_stream_t stream, bool with_combine) {
+                         mla_stream_t stream, bool with_combine, bool stall_test = false) {
   const mla_status_t chk = mla::check_decode_args(
       q, b, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride, block_table, max_blocks_per_seq,
       cache_seqlens, dv, metadata, num_parts, num_splits, softmax_scale, causal, out, lse, workspace,
@@ -228,6 +228,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   p.max_blocks = max_blocks_per_seq;
   p.causal = causal;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.stall_test = stall_test ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (mla::launch_decode(p, q_rope, k_lat, k_rope, num_parts, s.row_tiles, st) != cudaSuccess)
@@ -262,6 +263,18 @@ mla_status_t mla_decode_splitkv(const void* q, int b, int s_q, int h_q, int d, c
   return decode_impl(q, b, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride, block_table,
                      max_blocks_per_seq, cache_seqlens, dv, metadata, num_parts, num_splits,
                      softmax_scale, causal, out, lse, workspace, workspace_bytes, status, stream, false);
+}
+
+mla_status_t mla_selftest_wait_timeout(const void* q, int b, int s_q, int h_q, int d, const void* kcache,
+                                       int64_t num_blocks, int block_size, int h_kv, int stride,
+                                       const int32_t* block_table, int max_blocks_per_seq,
+                                       const int32_t* cache_seqlens, int dv, const int32_t* metadata,
+                                       int num_parts, const int32_t* num_splits, float softmax_scale, int causal,
+                                       void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                       int32_t* status, mla_stream_t stream) {
+  return decode_impl(q, b, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride, block_table,
+                     max_blocks_per_seq, cache_seqlens, dv, metadata, num_parts, num_splits, softmax_scale,
+                     causal, out, lse, workspace, workspace_bytes, status, stream, true, true);
 }
 
 mla_status_t mla_write_cache(const void* kv_c, int64_t kv_c_row_stride, const void* k_pe, int64_t k_pe_row_stride,

@@ -105,7 +105,8 @@ constexpr int kBarOFull = kBarPFull + 1;
 constexpr int kBarXFull = kBarOFull + 1;    // kXSlots
 constexpr int kBarXEmpty = kBarXFull + kXSlots;  // kXSlots: the peer has read the slot
 constexpr int kBarDone = kBarXEmpty + kXSlots;
-constexpr int kNumBars = kBarDone + 1;
+constexpr int kBarStall = kBarDone + 1;  // never completed: the wait-timeout diagnostic waits on it
+constexpr int kNumBars = kBarStall + 1;
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffLoFlag = kOffMisc + 16 + 4 * kXSlots;  // two words: page (by parity) + 1 when its low part runs
@@ -300,6 +301,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       mbar_init(bar(kBarXEmpty + s), 1);
     }
     mbar_init(bar(kBarDone), 3);    // the three MMA-issuing threads
+    mbar_init(bar(kBarStall), 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -329,6 +331,13 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   if (warp == 4) {
     // ================================================= TMA producer
     if (lane == 0) {
+      bool ok = true;
+      if (P.stall_test) {
+        // Diagnostic: a wait that nothing completes, before any copy is
+        // issued.  The bounded wait gives up, raises the abort flag and every
+        // other warp role leaves its own wait; the call reports a timeout.
+        ok = mbar_wait(bar(kBarStall), 0, abort_flag);
+      }
       tma_prefetch_desc(&q_rope);
       tma_prefetch_desc(&k_lat);
       tma_prefetch_desc(&k_rope);
@@ -342,7 +351,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       // The Q rows of every later segment of this part go to L2 now: a
       // segment's Q is staged only once the previous segment's QKs are done,
       // and read from HBM that staging stalled the pipeline for microseconds.
-      {
+      if (ok) {
         PageWalk ws = w;
         if (ws.valid) ws.next_segment();
         const uint8_t* const qb = static_cast<const uint8_t*>(P.q);
@@ -359,7 +368,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
       }
       int n = 0, seg = 0;
-      bool ok = true;
       while (w.valid && ok) {
         if (w.first()) {
           ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);

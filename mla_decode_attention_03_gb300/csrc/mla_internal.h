@@ -43,6 +43,7 @@ struct DecodeParams {
   int max_blocks;
   int causal;
   float scale_log2;   // softmax_scale * log2(e)
+  int stall_test;     // diagnostic: the TMA producer first waits on a barrier nothing completes
 };
 
 struct CombineParams {

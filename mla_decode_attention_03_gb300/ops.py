@@ -44,7 +44,7 @@ def load_library():
     lib.mla_workspace_bytes.argtypes = [I, I, I, I]
     lib.mla_get_metadata.restype = ctypes.c_int32
     lib.mla_get_metadata.argtypes = [P, I, I, P, P, P, P]
-    for name in ("mla_decode_with_kvcache", "mla_decode_splitkv"):
+    for name in ("mla_decode_with_kvcache", "mla_decode_splitkv", "mla_selftest_wait_timeout"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int32
         fn.argtypes = [P, I, I, I, I, P, I64, I, I, I, P, I, P, I, P, I, P, F, I, P, P, P, SZ, P, P]

@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
         "mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits",
         "mla_decode_with_kvcache_static", "mla_write_cache", "mla_copy_blocks",
         "mla_host_pipeline_create", "mla_host_pipeline_destroy", "mla_host_chunks",
-        "mla_host_scratch_bytes", "mla_decode_host"])
+        "mla_host_scratch_bytes", "mla_decode_host", "mla_selftest_wait_timeout"])
 
 
 def test_every_declared_symbol_is_exported(lib):

@@ -1,0 +1,41 @@
+"""Failure detection of the decode kernel on the GPU, without a GPU fault.
+
+Every wait in the decode kernel is bounded (about 2 s).  The diagnostic entry
+point mla_selftest_wait_timeout runs the decode with one wait on a barrier
+that nothing ever completes, placed before any copy is issued: the wait gives
+up, every warp role of both CTAs of each cluster leaves its own wait through
+the CTA's abort flag, and the status word reports MLA_ERR_TIMEOUT (-6).  The
+context must stay usable: a normal decode right after it matches the oracle.
+"""
+import pytest
+import torch
+
+from mla_decode_attention_03_gb300 import ops
+from mla_decode_attention_03_gb300 import workloads as W
+from tests._gpu_helpers import all_rows, assert_matches, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_that_never_ends_reports_timeout_and_context_survives():
+    w = W.make(2, 1, 128, 1, [100, 300], stride=640, seed=28)
+    dev = to_device(w)
+    status = ops.new_status()
+    parts = 4
+    meta, nsplit = ops.get_mla_metadata(dev["cache_seqlens"], parts, status)
+    out = torch.empty((w.b, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.b, 128, 1), dtype=torch.float32, device="cuda")
+    ws = torch.empty((ops.workspace_bytes(w.b, 1, 128, parts),), dtype=torch.uint8, device="cuda")
+    kc = dev["kcache"]
+    bt, sl = dev["block_table"], dev["cache_seqlens"]
+    rc = ops.load_library().mla_selftest_wait_timeout(
+        dev["q"].data_ptr(), w.b, 1, 128, 576, kc.data_ptr(), w.num_blocks, 64, 1, ops.entry_stride(kc),
+        bt.data_ptr(), bt.shape[1], sl.data_ptr(), 512, meta.data_ptr(), parts, nsplit.data_ptr(),
+        w.softmax_scale, 0, out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), status.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    # the context is still usable
+    o2, l2, _, _ = run_gpu(w, dev=dev)
+    assert_matches(w, o2, l2, all_rows(w))

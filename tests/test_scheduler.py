@@ -117,6 +117,8 @@ CASES = [
     ("short", list(np.random.default_rng(1).integers(1, 200, 300))),
     ("mtp", list(np.clip(np.round(np.random.default_rng(2).normal(4096, 1024, 128)), 256, 8192).astype(int))),
     ("long_one", [1 << 20]),
+    # more sequences than the single-warp path of the device scheduler takes
+    ("many", list(np.random.default_rng(3).integers(0, 3000, 3000))),
 ]
 
 
