@@ -48,7 +48,7 @@ MIN_TIMED_S = 1.0    # the timed loop lasts at least this long, so that clock sa
 # whose code changed since the capture reports null traffic.
 KERNEL_SOURCES = ("mla_decode.cu", "sm103_ptx.cuh", "mla_sched.cu", "mla_internal.h")
 MEASURED_TRAFFIC = {
-    ("451bb450dbfddd6b", "bench", 576): 626909184,
+    ("08d243f6a66d2961", "bench", 576): 627143680,
 }
 
 
@@ -621,6 +621,45 @@ def run_cache_ops(args):
                       "ms": round(ms, 5), "GB/s": round(nbytes / 1e6 / ms, 1), "bytes": nbytes}), flush=True)
 
 
+# Small cases of each workload for ncu captures with many passes: larger than
+# L2 (129 MB) so that DRAM counters mean something, a few hundred MB at most.
+NCU_CASES = {
+    "bench_full": lambda: W.named("bench"),
+    "bench32": lambda: W.make(32, 1, 128, 1, [4096] * 32, stride=576, seed=0, permute=False, name="bench32"),
+    "mtp32": lambda: W.make(32, 2, 128, 1,
+                            lambda r: np.clip(np.round(r.normal(4096.0, 1024.0, size=32)), 256, 8192),
+                            stride=640, causal=True, seed=0, name="mtp32"),
+    "skewed_s": lambda: W.make(64, 1, 128, 1,
+                               lambda r: np.concatenate([[49152, 49152], r.integers(64, 1024, size=62, endpoint=True)]),
+                               stride=640, seed=0, peaky_frac=0.01, name="skewed_s"),
+    "v2lite": lambda: W.named("v2lite"),
+}
+
+
+def run_ncu_case(args):
+    """Three L2-flushed passes of the hot path on one small case, for ncu
+    (capture the third decode launch with -k regex:mla_decode_kernel -s 2 -c 1)."""
+    from mla_decode_attention_03_gb300 import ops
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = NCU_CASES[args.ncu_case]()
+    q, kc = w.q.to(dev), w.kcache_alloc.to(dev)[..., :576]
+    bt, sl = w.block_table.to(dev), w.cache_seqlens.to(dev)
+    parts = ops.num_parts(w.s_q, w.h_q, w.h_kv, dev)
+    dec = ops.MLADecoder(w.b, w.s_q, w.h_q, w.h_kv, device=dev, parts=parts)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for k in range(3):
+        flush.fill_(k)
+        dec.plan(sl)
+        dec(q, kc, bt, sl, w.softmax_scale, w.causal)
+    torch.cuda.synchronize()
+    ops.check_status(dec.status)
+    nbytes, flops = metric_bytes_flops(w)
+    print(json.dumps({"mode": "ncu_case", "case": args.ncu_case, "workload": describe(w),
+                      "bytes_per_pass": nbytes, "flops_per_pass": flops}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -637,7 +676,12 @@ def main():
     ap.add_argument("--e2e-runs", default=None,
                     help="comma-separated run counts: also time the host-buffer step with each "
                          "(1 = copies in, decode, copies out one after another) and add them as e2e_runs")
+    ap.add_argument("--ncu-case", default=None, choices=sorted(NCU_CASES),
+                    help="run three passes of one small case for an ncu capture and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
