@@ -311,7 +311,7 @@ mla_status_t mla_host_pipeline_destroy(mla_host_pipeline *pipeline);
  * the running cost reaches k/n of the total, moved as needed so that every
  * run holds at least one sequence.  chunks >= 1 asks for that many runs
  * (capped at MLA_HOST_MAX_CHUNKS and at b); chunks <= 0 picks
- * n = total pages / 1024 clamped to [1, 4]: fewer, larger runs when the
+ * n = total pages / 2800, rounded, clamped to [1, 3]: fewer, larger runs when the
  * batch is small, so that the fixed cost of a run (a schedule, a pipeline
  * fill, a merge) stays small against its pages.
  */

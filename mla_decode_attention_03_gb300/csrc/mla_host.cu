@@ -47,11 +47,12 @@ struct mla_host_pipeline {
 
 namespace {
 
-// Automatic cut: one run per 1024 pages, at most 4 (measured on the benchmark's
-// workloads: b=128 x 64 pages best at 3-4 runs, two 1024-page sequences plus
-// short ones at 2, 16 short sequences at 1).
-constexpr int kAutoChunkPages = 1024;
-constexpr int kAutoMaxChunks = 4;
+// Automatic cut: total pages / 2800, rounded, clamped to [1, 3] (measured on the
+// benchmark's workloads: b=128 x 64 pages best at 2-3 runs, 128 causal s_q=2
+// sequences of ~66 pages best at 3-4, two 1024-page sequences plus 62 short
+// ones and 16 short sequences best at 1).
+constexpr int kAutoChunkPages = 2800;
+constexpr int kAutoMaxChunks = 3;
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -140,7 +141,7 @@ int mla_host_chunks(const int32_t* cache_seqlens, int b, int chunks, int32_t* bo
   const int64_t pages = total - b;
   int n = chunks;
   if (n <= 0) {
-    const int64_t a = pages / kAutoChunkPages;
+    const int64_t a = (pages + kAutoChunkPages / 2) / kAutoChunkPages;
     n = static_cast<int>(a < 1 ? 1 : (a > kAutoMaxChunks ? kAutoMaxChunks : a));
   }
   if (n > MLA_HOST_MAX_CHUNKS) n = MLA_HOST_MAX_CHUNKS;

@@ -84,7 +84,7 @@ def test_bench_workload_all_rows():
     automatic cut (the configuration its end-to-end figure times), every row."""
     w = W.named("bench")
     dev = to_device(w)
-    assert len(ops.host_chunks(w.cache_seqlens)) - 1 == 4
+    assert len(ops.host_chunks(w.cache_seqlens)) - 1 == 3
     hd = ops.HostDecoder(w.b, w.s_q, w.h_q, w.block_table.shape[1], w.h_kv)
     out, lse = run_host(w, hd, dev["kcache"], chunks=0)
     hd.close()
