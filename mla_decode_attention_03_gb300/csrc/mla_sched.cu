@@ -171,11 +171,13 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // One warp per (sequence, query row).  Sequences with a single split were
 // written directly by the decode kernel; sequences with none (length 0) get
 // out = 0 and lse = -inf.
-__global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams P) {
+constexpr int kCombineWarps = 4;  // rows per block, one warp each
+
+__global__ void __launch_bounds__(32 * kCombineWarps) mla_combine_kernel(const CombineParams P) {
   grid_dependency_wait();  // the decode kernel's partials are complete and visible
   const int i = blockIdx.x;
   const int rows = P.s_q * P.h_q;
-  const int row = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int row = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int s0 = P.num_splits[i];
@@ -184,6 +186,47 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams P)
   const int j = row / P.h_q, h = row - (row / P.h_q) * P.h_q;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) + (static_cast<int64_t>(i) * rows + row) * kDimV;
   float* lse_out = P.lse + (static_cast<int64_t>(i) * P.h_q + h) * P.s_q + j;
+
+  if (ns == 2) {
+    // The common cut (a sequence in two pieces): both pieces' lse and values
+    // are loaded in one round of loads, then merged.
+    const int64_t r0 = static_cast<int64_t>(s0) * rows + row, r1 = r0 + rows;
+    const float4* src0 = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r0 * kDimV) + lane * 4;
+    const float4* src1 = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r1 * kDimV) + lane * 4;
+    const float l0 = P.ws_lse[r0], l1 = P.ws_lse[r1];
+    float4 a[4], b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      a[q] = src0[q];
+      b[q] = src1[q];
+    }
+    const float m = fmaxf(l0, l1);
+    float lse2 = -INFINITY, w0 = 0.f, w1 = 0.f;
+    if (m != -INFINITY) {
+      const float e0 = expf(l0 - m), e1 = expf(l1 - m);
+      const float inv = 1.f / (e0 + e1);
+      w0 = e0 * inv;
+      w1 = e1 * inv;
+      lse2 = m + logf(e0 + e1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out) + lane * 2;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float4 x0 = a[2 * q], x1 = a[2 * q + 1], y0 = b[2 * q], y1 = b[2 * q + 1];
+      __nv_bfloat162 c0 = __floats2bfloat162_rn(w0 * x0.x + w1 * y0.x, w0 * x0.y + w1 * y0.y);
+      __nv_bfloat162 c1 = __floats2bfloat162_rn(w0 * x0.z + w1 * y0.z, w0 * x0.w + w1 * y0.w);
+      __nv_bfloat162 c2 = __floats2bfloat162_rn(w0 * x1.x + w1 * y1.x, w0 * x1.y + w1 * y1.y);
+      __nv_bfloat162 c3 = __floats2bfloat162_rn(w0 * x1.z + w1 * y1.z, w0 * x1.w + w1 * y1.w);
+      uint4 v;
+      v.x = *reinterpret_cast<uint32_t*>(&c0);
+      v.y = *reinterpret_cast<uint32_t*>(&c1);
+      v.z = *reinterpret_cast<uint32_t*>(&c2);
+      v.w = *reinterpret_cast<uint32_t*>(&c3);
+      dst[q] = v;
+    }
+    if (lane == 0) *lse_out = lse2;
+    return;
+  }
 
   float mx = -INFINITY;
   for (int k = lane; k < ns; k += 32) mx = fmaxf(mx, P.ws_lse[static_cast<int64_t>(s0 + k) * rows + row]);
@@ -254,8 +297,8 @@ cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   const int rows = p.s_q * p.h_q;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.b, (rows + 3) / 4, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.gridDim = dim3(p.b, (rows + kCombineWarps - 1) / kCombineWarps, 1);
+  cfg.blockDim = dim3(32 * kCombineWarps, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
