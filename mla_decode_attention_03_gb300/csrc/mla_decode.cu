@@ -45,7 +45,7 @@
 //    QK back until PV(n-3) had been issued, or prefetching S a page early, was
 //    measured slower and dropped.
 //  * P is rounded to bf16 for the tensor cores.  On pages where one weight
-//    exceeds a quarter of its row half's running sum, a second PV pass adds
+//    exceeds a third of its row's running sum, a second PV pass adds
 //    P_lo V (P_lo = the bf16 rounding error of P, itself in bf16), so cancelling
 //    value rows under a few dominant keys stay within the tolerance.
 //  * Exchange slots are returned to the sender by an explicit credit: each
@@ -127,10 +127,12 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // A page gets a second PV pass with the bf16 rounding error of P (P - bf16(P),
-// itself in bf16) when one of its weights exceeds a quarter of the running sum
-// of its row half: 3 * e > l_prev.  Such weights carry enough of the output
+// itself in bf16) when one of its weights exceeds a third of its row's running
+// sum, this page included: 3 * e > l.  Such weights carry enough of the output
 // that the 2^-9 relative rounding of P alone could move an output element by
-// more than the tolerance when value rows cancel.
+// more than the tolerance when value rows cancel.  (Many weights of similar
+// size, as on the first page of a segment, round independently and need no
+// second pass.)
 constexpr float kLoRatio = 3.0f;
 constexpr float kQuantMax = 32767.0f;
 // q in [-32767, 32767] travels as the low 16 bits of the fp32 value
@@ -230,6 +232,84 @@ __device__ __noinline__ void rescale_o_half(uint32_t t_o, float alpha) {
 #pragma unroll
     for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
     tmem_st16x2(t_o + 32u * c, o);
+  }
+}
+
+// In-register transpose of 16-byte blocks within each group of G lanes (G = 4
+// or 8): lane G*a + m enters with the G blocks b[4j .. 4j+3] of its own output
+// line and leaves with block m of the lines of lanes G*a + [0, G), in lane
+// order.  log2(G) butterfly steps; each swaps the half of the blocks whose
+// index differs from the lane in one bit with the partner lane across it.
+template <int G>
+__device__ __forceinline__ void transpose_blocks(uint32_t (&b)[4 * G], int lane) {
+#pragma unroll
+  for (int bit = G / 2; bit >= 1; bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int j0 = 0; j0 < G; ++j0) {
+      if (j0 & bit) continue;
+      const int j1 = j0 | bit;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, up ? b[4 * j0 + e] : b[4 * j1 + e], bit);
+        if (up)
+          b[4 * j0 + e] = recv;
+        else
+          b[4 * j1 + e] = recv;
+      }
+    }
+  }
+}
+
+// Writes this warp's 16 rows of the CTA's O half (tensor memory from `t_o`),
+// scaled by each row's 1/l, to global memory: bf16 into `out_b` or fp32 into
+// `out_f` (row r of the segment at element r * kDimV, this CTA's half at
+// `col0`).  Lane l holds row l & 15, columns 32 * (l >> 4) + [0, 32) of a
+// 64-column chunk; a transpose within groups of lanes lets every store
+// instruction write four whole 128-byte lines instead of touching 32 lines
+// with 16 bytes each.  Rows whose bit in `live` is clear are not written.
+__device__ __noinline__ void write_o_rows(uint32_t t_o, float inv_l, __nv_bfloat16* out_b, float* out_f, int col0,
+                                          int row_in_seq, uint32_t live) {
+  const int lane = static_cast<int>(lane_id());
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    tmem_ld16x2_32(t_o + 64u * c, o);
+    tmem_wait_ld(o);
+    if (out_b != nullptr) {
+      // a line is one row's 64 columns (two lanes' 64 bytes): groups of four
+      // lanes hold four rows of one half; lanes 4a+m and 4(a+4)+m write the
+      // two halves of row 4(a & 3) + k
+      uint32_t b[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        b[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+      transpose_blocks<4>(b, lane);
+      const int a = lane >> 2, m = lane & 3;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rs = 4 * (a & 3) + k;
+        const int64_t r = __shfl_sync(0xffffffffu, row_in_seq, rs);
+        if ((live >> rs) & 1u)
+          *reinterpret_cast<uint4*>(out_b + r * kDimV + col0 + 64 * c + 32 * (a >> 2) + 8 * m) =
+              make_uint4(b[4 * k], b[4 * k + 1], b[4 * k + 2], b[4 * k + 3]);
+      }
+    } else {
+      // a line is one row's 32 columns of one half (one lane's 128 bytes):
+      // groups of eight lanes hold eight rows of one half
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+      transpose_blocks<8>(o, lane);
+      const int a = lane >> 3, m = lane & 7;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rs = 8 * (a & 1) + k;
+        const int64_t r = __shfl_sync(0xffffffffu, row_in_seq, rs);
+        if ((live >> rs) & 1u)
+          *reinterpret_cast<uint4*>(out_f + r * kDimV + col0 + 64 * c + 32 * (a >> 1) + 4 * m) =
+              make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+      }
+    }
   }
 }
 
@@ -338,7 +418,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         // other warp role leaves its own wait; the call reports a timeout.
         ok = mbar_wait(bar(kBarStall), 0, abort_flag);
       }
-      tma_prefetch_desc(&q_rope);
       tma_prefetch_desc(&k_lat);
       tma_prefetch_desc(&k_rope);
       const uint64_t evict_first = l2_policy_evict_first();
@@ -367,16 +446,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
           }
         }
       }
-      int n = 0, seg = 0;
+      // K pages need no Q: the loads run on across segment boundaries (a
+      // segment's Q rope quarter is loaded by the Q-staging warps).
+      int n = 0;
       while (w.valid && ok) {
-        if (w.first()) {
-          ok = mbar_wait(bar(kBarQEmpty), (seg & 1) ^ 1, abort_flag);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bar(kBarQFull), static_cast<uint32_t>(rows_valid) * 64u);
-          tma_load_4d(base + kOffQR, &q_rope, bar(kBarQFull), dim_rope, g * P.heads_per_kv,
-                      tile * P.q_per_tile, w.i);
-          ++seg;
-        }
         int phys = __ldg(P.block_table + static_cast<int64_t>(w.i) * P.max_blocks + w.p);
         if (phys < 0 || phys >= P.num_blocks) {
           raise_status(P.status, kStatusBadBlockId);
@@ -401,7 +474,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         // let the copies already issued land before this CTA can exit
         for (int m = (n > kStages ? n - kStages : 0); m < n; ++m)
           drain_wait(bar(kBarFull + m % kStages), (m / kStages) & 1);
-        if (seg > 0) drain_wait(bar(kBarQFull), (seg - 1) & 1);
       }
     }
     __syncwarp();
@@ -663,9 +735,6 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
       }
       const float neg_mc = (m_run == -INFINITY) ? 0.f : -m_run * c_log2;
-      // Does a weight of this warp's lanes exceed a quarter of its running sum?
-      // (-inf lanes give 0, NaN compares false.)
-      const bool want_lo = __any_sync(0xffffffffu, ex2_approx(fmaf(mx_lane, c_log2, neg_mc)) * kLoRatio > l_run * alpha);
       uint32_t pk[16];
       float rsum;
       {
@@ -688,6 +757,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         rsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       }
       l_run = l_run * alpha + rsum;  // this lane's 32 tokens; the row sum adds lane l^16's
+      // Does a weight of this warp's rows exceed a third of its row's sum so
+      // far?  (-inf lanes give 0, NaN compares false.)
+      const bool want_lo =
+          __any_sync(0xffffffffu, ex2_approx(fmaf(mx_lane, c_log2, neg_mc)) * kLoRatio >
+                                      l_run + __shfl_xor_sync(0xffffffffu, l_run, 16));
 
       // The previous page's low part, if any warp asked for it: once its bf16
       // part's PV is complete (it read the P buffer), every warp stores its own
@@ -751,39 +825,15 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
         const float lse = (l_tot > 0.f) ? (m_run * c_log2 + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
         const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + w.i)) + w.k;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          // columns [64c, 64c+64) of this CTA's half: lane l takes 32 of them
-          uint32_t o[32];
-          tmem_ld16x2_32(tmem + lane_off + kTmemO + 64u * c, o);
-          tmem_wait_ld(o);
-          if (row_live) {
-            const int col = 256 * static_cast<int>(rank) + 64 * c + 32 * (lane_i >> 4);
-            if (direct) {
-              // single-split sequences go straight to out (bf16)
-              uint4* dstp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.out) +
-                                                     ((static_cast<int64_t>(w.i) * rows_total + row_in_seq) * kDimV + col));
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-                v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-                v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-                v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-                dstp[q] = v;
-              }
-            } else {
-              // the pieces of the others go to the workspace, fp32, each
-              // normalised by its own sum
-              float4* dstp = reinterpret_cast<float4*>(static_cast<float*>(P.ws_o) +
-                                                       ((oslot * rows_total + row_in_seq) * kDimV + col));
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dstp[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                      __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
-            }
-          }
-        }
+        const uint32_t live = __ballot_sync(0xffffffffu, row_live);
+        if (direct)
+          write_o_rows(tmem + lane_off + kTmemO, inv_l,
+                       static_cast<__nv_bfloat16*>(P.out) + static_cast<int64_t>(w.i) * rows_total * kDimV, nullptr,
+                       256 * static_cast<int>(rank), row_in_seq, live);
+        else
+          write_o_rows(tmem + lane_off + kTmemO, inv_l, nullptr,
+                       static_cast<float*>(P.ws_o) + oslot * rows_total * kDimV, 256 * static_cast<int>(rank),
+                       row_in_seq, live);
         if (row_live && rank == 0 && lane_i < 16) {
           if (direct)
             P.lse[(static_cast<int64_t>(w.i) * P.h_q + h) * P.s_q + j] = lse;
@@ -806,9 +856,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     // writes it with st.async into the peer's receive slot, at the place of
     // the peer softmax thread that owns the row, once the peer has returned
     // that slot: they, not the softmax warps, do the quantisation and absorb
-    // the SM-to-SM link's back-pressure.  A segment's Q is staged as soon as
-    // the previous segment's QKs are done, and at the latest before its first
-    // page is sent.
+    // the SM-to-SM link's back-pressure.  A segment's Q is staged once the
+    // previous segment's QKs are done (warp 0 also starts the TMA load of its
+    // rope quarter then), and before its first page can be sent.
     const int quad = warp & 3;
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
@@ -820,6 +870,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(P.q);
     const uint32_t peer_x = cluster_map(base + kOffX, peer);
     const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
+    const int dim_rope = 512 + 32 * static_cast<int>(rank);
     int lim = 0;  // visible tokens of this row in the current sequence
 
     auto load32 = [&](const uint8_t* src, uint32_t (&r)[32]) {
@@ -849,12 +900,18 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       load32(src, q0);
       load32(src + 128, q1);
       if (!mbar_wait(bar(kBarQEmpty), (qseg & 1) ^ 1, abort_flag)) return false;
+      if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(bar(kBarQFull), static_cast<uint32_t>(rows_valid) * 64u);
+        tma_load_4d(base + kOffQR, &q_rope, bar(kBarQFull), dim_rope, g * P.heads_per_kv, tile * P.q_per_tile,
+                    wq.i);
+      }
       tc_fence_after_sync();
       tmem_st32(tmem + lane_off + kTmemQ, q0);
       tmem_st32(tmem + lane_off + kTmemQ + 32, q1);
+      // the second half in one round of loads
       load32(src + 256, q0);
-      tmem_st32(tmem + lane_off + kTmemQ + 64, q0);
       load32(src + 384, q1);
+      tmem_st32(tmem + lane_off + kTmemQ + 64, q0);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         *reinterpret_cast<uint4*>(gbase + kOffQL + row * 128 + ((k ^ (row & 7)) << 4)) =
@@ -868,20 +925,23 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       wq.next_segment();
       return true;
     };
-    // The warps poll: a segment's Q is staged the moment the previous
-    // segment's QKs are done (its first page's QK waits for it), otherwise the
-    // next page is sent once its S is ready.  Staging never waits behind a
-    // send, whose slot credit depends on the peer's progress.  Each decision is
-    // lane 0's, broadcast, so the warp stays converged.
+    // The warps poll: the next page is sent as soon as its S is ready (the
+    // peer's softmax waits for it); otherwise a segment's Q is staged once the
+    // previous segment's QKs are done (the next segment's first QK waits for
+    // it, and its K pages are still in flight).  A send waits only for the
+    // peer's progress on earlier pages, so this order cannot deadlock.  Each
+    // decision is lane 0's, broadcast, so the warp stays converged.
     int n = 0;
     long long t_idle = clock64();
     while (ok && (w.valid || wq.valid)) {
-      if (__shfl_sync(0xffffffffu, (wq.valid && mbar_test(bar(kBarQEmpty), (qseg & 1) ^ 1)) ? 1 : 0, 0)) {
+      const bool s_ready =
+          __shfl_sync(0xffffffffu, (w.valid && mbar_test(bar(kBarSFull + (n & 1)), (n >> 1) & 1)) ? 1 : 0, 0) != 0;
+      if (!s_ready && __shfl_sync(0xffffffffu, (wq.valid && mbar_test(bar(kBarQEmpty), (qseg & 1) ^ 1)) ? 1 : 0, 0)) {
         ok = stage_q();
         t_idle = clock64();
         continue;
       }
-      if (!w.valid || !__shfl_sync(0xffffffffu, mbar_test(bar(kBarSFull + (n & 1)), (n >> 1) & 1) ? 1 : 0, 0)) {
+      if (!s_ready) {
         if (w.valid) mbar_try_wait_for(bar(kBarSFull + (n & 1)), (n >> 1) & 1, 200);
         else mbar_try_wait_for(bar(kBarQEmpty), (qseg & 1) ^ 1, 200);
         int give_up = (*abort_flag || clock64() - t_idle > kWaitTimeoutCycles) ? 1 : 0;
@@ -940,7 +1000,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       }
       const int slot = n % kXSlots;
       if (n >= kXSlots) {
-        // the peer has read page n - 2 out of the slot page n goes to
+        // the peer has read page n - kXSlots out of the slot page n goes to
         ok = mbar_wait<true>(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, abort_flag);
         if (!ok) break;
       }
@@ -961,7 +1021,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       ++n;
       w.advance();
     }
-    if (!ok) raise_status(P.status, kStatusTimeout);
+    if (!ok) {
+      raise_status(P.status, kStatusTimeout);
+      // let the last rope load land before this CTA can exit
+      if (warp == 0 && lane == 0 && qseg > 0) drain_wait(bar(kBarQFull), (qseg - 1) & 1);
+    }
   }
 
   // ---- teardown: everyone is done with tensor memory and with the peer
