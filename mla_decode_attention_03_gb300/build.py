@@ -49,8 +49,10 @@ def build(force: bool = False, verbose: bool = False) -> Path:
     if verbose:
         common += ["-Xptxas", "-v"]
 
+    # object and library names carry the process id, so that builds started at
+    # the same time (parallel test workers) never read each other's files
     def compile_one(src: str) -> Path:
-        obj = BUILD / (Path(src).stem + ".o")
+        obj = BUILD / f"{Path(src).stem}.{os.getpid()}.o"
         cmd = [cc, "-c", str(CSRC / src), "-o", str(obj)] + common
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,6 +66,8 @@ def build(force: bool = False, verbose: bool = False) -> Path:
     tmp = LIB.with_suffix(f".{os.getpid()}.tmp")
     cmd = [cc, "-shared", "-o", str(tmp)] + [str(o) for o in objs] + ARCH + ["-lcudart_static", "-ldl", "-lrt", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
+    for o in objs:
+        o.unlink(missing_ok=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
