@@ -74,6 +74,10 @@ constexpr int kFirstSoftmaxWarp = 8;
 constexpr uint32_t kRegsIssue = 48;
 constexpr uint32_t kRegsStage = 120;
 constexpr uint32_t kRegsSoftmax = 168;
+// setmaxnreg.inc waits until the registers it asks for are free: the three
+// shares must fit in what the block was launched with (128 per thread).
+static_assert(128 * kRegsIssue + 128 * kRegsStage + 256 * kRegsSoftmax <= kThreads * 128u,
+              "register split exceeds the launch allocation");
 // A K stage is held from its TMA issue (about 1.3 us of HBM latency under
 // load) until the PV of its page has read V, so the number of stages bounds the
 // pages in flight; five stages and a single exchange slot fill the 227 KB.
