@@ -88,6 +88,7 @@ constexpr int kKStage = 4 * kKChunk + kKRope;  // 36864 bytes: this CTA's 288 di
 constexpr int kXSlots = 1;     // receive slots (peer partials)
 constexpr int kXData = kRowsPerTile * 128;     // 128 rows x 64 int16 (two 32-token halves)
 constexpr int kXSlot = kXData + 2 * kRowsPerTile * 4;  // + one fp32 scale per (row, half)
+constexpr int kXRowBytes = kXSlot / kRowsPerTile;      // one row's share: 136 bytes
 constexpr int kQRope = kRowsPerTile * 64;      // Q rope quarter: 128 rows x 32 bf16 (64B swizzle)
 constexpr int kQLat = kRowsPerTile * 128;      // Q latent dims [192, 256) of the CTA: 128 rows x 64 bf16
 
@@ -361,6 +362,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
   const int g = blockIdx.z;
   const int32_t* meta = P.metadata + part * kMetaInts;
   const int rows_valid = P.rows_per_tile;
+  // Rows of this tile that belong to a query position: a prefix of the tile.
+  // Only they are exchanged (a tile of 16 heads sends an eighth of the bytes).
+  const int rows_live = min(rows_valid, (P.s_q - tile * P.q_per_tile) * P.heads_per_kv);
 
   // ---- setup
   if (tid == 0) {
@@ -632,6 +636,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const int j = tile * P.q_per_tile + jj;
     const int h = g * P.heads_per_kv + hh;
     const bool row_live = (row < rows_valid) && (j < P.s_q);
+    // A warp whose 16 rows hold no query position keeps the hand-offs but
+    // skips the peer's partial (none is sent for those rows).  Its scores are
+    // never written out; rows are independent in every step, so whatever they
+    // hold cannot reach a live row.
+    const bool warp_live = 32 * quad + 16 * half < rows_live;
     const int rows_total = P.s_q * P.h_q;
     const int row_in_seq = j * P.h_q + h;
     // Scores stay in raw units (q.k); scale*log2(e) is applied inside the exp2
@@ -659,7 +668,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       // quantise and send the same partial to the peer meanwhile)
       const int sb = n & 1;
       const int slot = n % kXSlots;
-      if (leader) mbar_arrive_expect_tx(bar(kBarXFull + slot), kXSlot);
+      if (leader) mbar_arrive_expect_tx(bar(kBarXFull + slot), static_cast<uint32_t>(rows_live) * kXRowBytes);
       ok = mbar_wait(bar(kBarSFull + sb), (n >> 1) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
@@ -678,7 +687,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       // ======== add the peer's partial
       ok = mbar_wait(bar(kBarXFull + slot), (n / kXSlots) & 1, abort_flag);
       if (!ok) break;
-      {
+      if (warp_live) {
         const uint8_t* xr = gbase + kOffX + slot * kXSlot;
         const float sc = *reinterpret_cast<const float*>(xr + x_scale(sw, lane_i));
         const uint64_t sc2 = f2(sc, sc), nbase2 = f2(-kQuantBase, -kQuantBase);
@@ -874,6 +883,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(P.q);
     const uint32_t peer_x = cluster_map(base + kOffX, peer);
     const uint32_t peer_xfull = cluster_map(bar(kBarXFull), peer);
+    // A warp with no live row writes nothing into the peer's slot, so it does
+    // not wait for the slot's credit either: the credit's phases follow the
+    // warps that send, and a waiter that fell two phases behind them would
+    // wait on the wrong phase.
+    const bool sends = __any_sync(0xffffffffu, row_live);
     const int dim_rope = 512 + 32 * static_cast<int>(rank);
     int lim = 0;  // visible tokens of this row in the current sequence
 
@@ -1003,7 +1017,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         scl[th] = amax * (1.0f / kQuantMax);
       }
       const int slot = n % kXSlots;
-      if (n >= kXSlots) {
+      if (sends && n >= kXSlots) {
         // the peer has read page n - kXSlots out of the slot page n goes to
         ok = mbar_wait<true>(bar(kBarXEmpty + slot), ((n / kXSlots) - 1) & 1, abort_flag);
         if (!ok) break;
@@ -1015,6 +1029,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
       const int rsw = quad + 4 * static_cast<int>(lane >> 4);
 #pragma unroll
       for (int th = 0; th < 2; ++th) {
+        if (!row_live) break;  // rows past the tile's query positions are not exchanged
         const int rl = static_cast<int>(lane & 15) + 16 * th;
 #pragma unroll
         for (int k = 0; k < 4; ++k)

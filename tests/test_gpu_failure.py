@@ -39,3 +39,30 @@ def test_wait_that_never_ends_reports_timeout_and_context_survives():
     # the context is still usable
     o2, l2, _, _ = run_gpu(w, dev=dev)
     assert_matches(w, o2, l2, all_rows(w))
+
+
+@pytest.mark.parametrize("name", ["v2lite", "tiny"])
+def test_small_head_tiles_repeated_back_to_back(name):
+    """Tiles with fewer live rows than 128 (16 heads) exchange only their live
+    rows, and the sender warps without a live row skip the slot credit.  A
+    waiter that could fall two phases behind the credit would show up only
+    after several back-to-back decodes (a timeout, not a fault): 40 of them,
+    with the status word checked after every one and the last output compared
+    with the oracle on every row."""
+    w = W.named(name)
+    dev = to_device(w)
+    parts = ops.num_parts(w.s_q, w.h_q, w.h_kv)
+    dec = ops.MLADecoder(w.b, w.s_q, w.h_q, w.h_kv, parts=parts)
+    meta, nsplit = ops.get_mla_metadata(dev["cache_seqlens"], parts, dec.status)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for k in range(40):
+        flush.fill_(k)
+        out, lse = ops.mla_decode_with_kvcache(dev["q"], dev["kcache"], dev["block_table"], dev["cache_seqlens"],
+                                               meta, nsplit, w.softmax_scale, w.causal, workspace=dec.workspace,
+                                               status=dec.status)
+        if k % 8 == 7:
+            torch.cuda.synchronize()
+            assert int(dec.status.item()) == 0, f"decode {k}: status {int(dec.status.item())}"
+    torch.cuda.synchronize()
+    assert int(dec.status.item()) == 0
+    assert_matches(w, out, lse, all_rows(w))
