@@ -48,7 +48,7 @@ MIN_TIMED_S = 1.0    # the timed loop lasts at least this long, so that clock sa
 # whose code changed since the capture reports null traffic.
 KERNEL_SOURCES = ("mla_decode.cu", "sm103_ptx.cuh", "mla_sched.cu", "mla_internal.h")
 MEASURED_TRAFFIC = {
-    ("63fd5c0a0d19cf15", "bench", 576): 626745856,
+    ("de489b54d6bf90cb", "bench", 576): 626740224,
 }
 
 
