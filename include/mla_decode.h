@@ -351,8 +351,10 @@ size_t mla_host_scratch_bytes(int b, int s_q, int h_q, int max_blocks_per_seq, i
  * not 256-byte aligned, b above 16384, and any cache_seqlens entry outside
  * [0, max_blocks_per_seq*64] (checked on the host, since the lengths are
  * there).  A CUDA call that fails part-way
- * returns MLA_ERR_CUDA with the runs before it already enqueued.  Not meant
- * for stream capture.
+ * returns MLA_ERR_CUDA with the runs before it already enqueued; the copies
+ * already queued on the pipeline's own streams are still joined into `stream`
+ * (as far as the failing CUDA state allows), so synchronising `stream` still
+ * waits for every write into out and lse.  Not meant for stream capture.
  */
 mla_status_t mla_decode_host(mla_host_pipeline *pipeline, const void *q, int b, int s_q, int h_q,
                              int d, const void *kcache, int64_t num_blocks, int block_size,

@@ -234,46 +234,58 @@ mla_status_t mla_decode_host(mla_host_pipeline* pipeline, const void* q, int b, 
   const bool split = n > 1;
   cudaStream_t in_s = split ? P->in : cs;
   cudaStream_t out_s = split ? P->out : cs;
-  if (split) {
-    MLA_CUDA(cudaEventRecord(P->start, cs));
-    MLA_CUDA(cudaStreamWaitEvent(P->in, P->start, 0));
-    MLA_CUDA(cudaStreamWaitEvent(P->out, P->start, 0));
-  }
-  // the previous call on this pipeline has finished (implied by stream order on the same caller stream)
-  if (P->has_prev && P->prev_stream != cs) MLA_CUDA(cudaStreamWaitEvent(in_s, P->done, 0));
-  for (int k = 0; k < n; ++k) {
-    const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
-    MLA_CUDA(cudaMemcpyAsync(q_d + i0 * q_row, qh + i0 * q_row, bk * q_row, cudaMemcpyHostToDevice, in_s));
-    MLA_CUDA(cudaMemcpyAsync(reinterpret_cast<char*>(bt_d) + i0 * bt_row, bth + i0 * bt_row, bk * bt_row,
-                             cudaMemcpyHostToDevice, in_s));
-    MLA_CUDA(cudaMemcpyAsync(sl_d + i0, cache_seqlens + i0, bk * sizeof(int32_t), cudaMemcpyHostToDevice, in_s));
-    const mla_status_t r = mla_get_metadata(sl_d + i0, bk, num_parts, meta_of(k), nsplit_of(k), status, in_s);
-    if (r != MLA_OK) return r;
-    if (split) MLA_CUDA(cudaEventRecord(P->in_ready[k], in_s));
-  }
-  for (int k = 0; k < n; ++k) {
-    const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
-    if (split) MLA_CUDA(cudaStreamWaitEvent(cs, P->in_ready[k], 0));
-    const mla_status_t r = mla_decode_with_kvcache(
-        q_d + i0 * q_row, bk, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride,
-        reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(bt_d) + i0 * bt_row), max_blocks_per_seq,
-        sl_d + i0, dv, meta_of(k), num_parts, nsplit_of(k), softmax_scale, causal, out_d + i0 * o_row,
-        reinterpret_cast<float*>(reinterpret_cast<char*>(lse_d) + i0 * l_row), ws, L.ws_bytes, status, stream);
-    if (r != MLA_OK) return r;
+  auto enqueue = [&]() -> mla_status_t {
     if (split) {
-      MLA_CUDA(cudaEventRecord(P->out_ready[k], cs));
-      MLA_CUDA(cudaStreamWaitEvent(P->out, P->out_ready[k], 0));
+      MLA_CUDA(cudaEventRecord(P->start, cs));
+      MLA_CUDA(cudaStreamWaitEvent(P->in, P->start, 0));
+      MLA_CUDA(cudaStreamWaitEvent(P->out, P->start, 0));
     }
-    MLA_CUDA(cudaMemcpyAsync(oh + i0 * o_row, out_d + i0 * o_row, bk * o_row, cudaMemcpyDeviceToHost, out_s));
-    MLA_CUDA(cudaMemcpyAsync(lh + i0 * l_row, reinterpret_cast<char*>(lse_d) + i0 * l_row, bk * l_row,
-                             cudaMemcpyDeviceToHost, out_s));
+    // the previous call on this pipeline has finished (implied by stream order on the same caller stream)
+    if (P->has_prev && P->prev_stream != cs) MLA_CUDA(cudaStreamWaitEvent(in_s, P->done, 0));
+    for (int k = 0; k < n; ++k) {
+      const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
+      MLA_CUDA(cudaMemcpyAsync(q_d + i0 * q_row, qh + i0 * q_row, bk * q_row, cudaMemcpyHostToDevice, in_s));
+      MLA_CUDA(cudaMemcpyAsync(reinterpret_cast<char*>(bt_d) + i0 * bt_row, bth + i0 * bt_row, bk * bt_row,
+                               cudaMemcpyHostToDevice, in_s));
+      MLA_CUDA(cudaMemcpyAsync(sl_d + i0, cache_seqlens + i0, bk * sizeof(int32_t), cudaMemcpyHostToDevice, in_s));
+      const mla_status_t r = mla_get_metadata(sl_d + i0, bk, num_parts, meta_of(k), nsplit_of(k), status, in_s);
+      if (r != MLA_OK) return r;
+      if (split) MLA_CUDA(cudaEventRecord(P->in_ready[k], in_s));
+    }
+    for (int k = 0; k < n; ++k) {
+      const int i0 = bounds[k], bk = bounds[k + 1] - bounds[k];
+      if (split) MLA_CUDA(cudaStreamWaitEvent(cs, P->in_ready[k], 0));
+      const mla_status_t r = mla_decode_with_kvcache(
+          q_d + i0 * q_row, bk, s_q, h_q, d, kcache, num_blocks, block_size, h_kv, stride,
+          reinterpret_cast<const int32_t*>(reinterpret_cast<const char*>(bt_d) + i0 * bt_row), max_blocks_per_seq,
+          sl_d + i0, dv, meta_of(k), num_parts, nsplit_of(k), softmax_scale, causal, out_d + i0 * o_row,
+          reinterpret_cast<float*>(reinterpret_cast<char*>(lse_d) + i0 * l_row), ws, L.ws_bytes, status, stream);
+      if (r != MLA_OK) return r;
+      if (split) {
+        MLA_CUDA(cudaEventRecord(P->out_ready[k], cs));
+        MLA_CUDA(cudaStreamWaitEvent(P->out, P->out_ready[k], 0));
+      }
+      MLA_CUDA(cudaMemcpyAsync(oh + i0 * o_row, out_d + i0 * o_row, bk * o_row, cudaMemcpyDeviceToHost, out_s));
+      MLA_CUDA(cudaMemcpyAsync(lh + i0 * l_row, reinterpret_cast<char*>(lse_d) + i0 * l_row, bk * l_row,
+                               cudaMemcpyDeviceToHost, out_s));
+    }
+    MLA_CUDA(cudaEventRecord(P->done, out_s));
+    if (split) MLA_CUDA(cudaStreamWaitEvent(cs, P->done, 0));
+    return MLA_OK;
+  };
+  const mla_status_t r = enqueue();
+  if (r != MLA_OK && split) {
+    // Something failed after work may already be queued on the side streams:
+    // join them into the caller's stream anyway (best effort), so that no copy
+    // of this call can still be writing the caller's buffers after its stream
+    // has passed this point, and the next call waits for them.
+    if (cudaEventRecord(P->done, in_s) == cudaSuccess) cudaStreamWaitEvent(out_s, P->done, 0);
+    if (cudaEventRecord(P->done, out_s) == cudaSuccess) cudaStreamWaitEvent(cs, P->done, 0);
   }
-  MLA_CUDA(cudaEventRecord(P->done, out_s));
-  if (split) MLA_CUDA(cudaStreamWaitEvent(cs, P->done, 0));
   P->has_prev = true;
   P->prev_stream = cs;
 #undef MLA_CUDA
-  return MLA_OK;
+  return r;
 }
 
 }  // extern "C"
