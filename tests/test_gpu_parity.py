@@ -29,6 +29,10 @@ SMALL = [
     ("empty_sequences", 3, 1, 128, 1, [0, 100, 0], 640, False, None),
     ("long_split_many", 2, 1, 128, 1, [5000, 3000], 640, False, None),
     ("h16_many_short", 40, 1, 16, 1, "short", 576, False, None),
+    # the last row tile only partly holds query positions (64 of 128 rows; 48
+    # of 96 with 48 heads): only those rows are exchanged between the CTAs
+    ("partial_last_tile", 3, 3, 64, 1, [100, 300, 65], 640, True, None),
+    ("h48_partial_last_tile", 2, 3, 48, 1, [200, 77], 576, True, 3),
 ]
 
 
