@@ -307,9 +307,12 @@ mla_status_t mla_host_pipeline_destroy(mla_host_pipeline *pipeline);
  * n + 1 sequence indices 0 = bounds[0] < bounds[1] < ... < bounds[n] = b into
  * `bounds` (room for MLA_HOST_MAX_CHUNKS + 1) and returns n, or a negative
  * mla_status_t for b < 1 or NULL pointers.  Sequence i costs
- * ceil(max(L_i, 0) / 64) + 1 units; run k ends at the first sequence where
- * the running cost reaches k/n of the total, moved as needed so that every
- * run holds at least one sequence.  chunks >= 1 asks for that many runs
+ * ceil(max(L_i, 0) / 64) + 1 units.  The first and the last run take half the
+ * share of a middle run (shares 1, 2, ..., 2, 1 in halves of a share; two runs
+ * share evenly), because their copies in and out have no decode to overlap:
+ * run k ends at the first sequence where the running cost reaches
+ * (2k - 1) / (2n - 2) of the total (k / 2 with two runs), moved as needed so
+ * that every run holds at least one sequence.  chunks >= 1 asks for that many runs
  * (capped at MLA_HOST_MAX_CHUNKS and at b); chunks <= 0 picks
  * n = total pages / 2800, rounded, clamped to [1, 3]: fewer, larger runs when the
  * batch is small, so that the fixed cost of a run (a schedule, a pipeline

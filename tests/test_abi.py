@@ -126,12 +126,15 @@ def _check_cut(seqlens, n, bounds):
     prefix = [0]
     for c in costs:
         prefix.append(prefix[-1] + c)
+    halves = n if n <= 2 else 2 * n - 2  # shares 1, 2, ..., 2, 1 in halves
     for k in range(1, n):
         e = bounds[k]
-        target = -(-total * k // n)
+        before = k if n <= 2 else 2 * k - 1
+        target = -(-total * before // halves)
         lo, hi = bounds[k - 1] + 1, b - (n - k)
         if lo < e < hi:
-            # an unclamped bound is the first sequence where the running cost reaches k/n of the total
+            # an unclamped bound is the first sequence where the running cost
+            # reaches its share of the total (end runs half a middle run)
             assert prefix[e] >= target and prefix[e - 1] < target, (k, e, target)
 
 
@@ -149,10 +152,12 @@ def test_host_chunks_cut(lib, seqlens, chunks, want_n):
     _check_cut(seqlens, n, bounds)
 
 
-def test_host_chunks_uniform_batch_cuts_evenly(lib):
-    for n_req in (2, 4, 8):
-        n, bounds = _chunks(lib, [4096] * 128, n_req)
-        assert bounds == [128 * k // n_req for k in range(n_req + 1)]
+def test_host_chunks_uniform_batch_end_runs_half(lib):
+    # 128 equal sequences: two runs split evenly; with more, the first and the
+    # last run hold half as many sequences as each middle run
+    assert _chunks(lib, [4096] * 128, 2)[1] == [0, 64, 128]
+    assert _chunks(lib, [4096] * 128, 3)[1] == [0, 32, 96, 128]
+    assert _chunks(lib, [4096] * 128, 5)[1] == [0, 16, 48, 80, 112, 128]
 
 
 def test_host_chunks_random_batches(lib):
