@@ -181,7 +181,7 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   const Shape s = tile_shape(s_q, h_q, h_kv);
   CUtensorMap q_rope, k_lat, k_rope;
   {
-    // the rope quarter of each CTA's Q columns; the latent half is read by the kernel's threads
+    // the 32 rope dims of each CTA's Q columns; its latent dims are read by the kernel's threads
     const cuuint64_t row = static_cast<cuuint64_t>(kDimQK) * 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(h_q),
                           static_cast<cuuint64_t>(s_q), static_cast<cuuint64_t>(b)};

@@ -28,7 +28,7 @@
 //  * Tensor memory per CTA: O half (256 columns), two S buffers (64 columns
 //    each), one P buffer (32 columns of packed bf16 that feed PV straight from
 //    tensor memory) and 192 of the CTA's 256 latent Q dims (96 columns); the
-//    other 64 latent Q dims and the rope quarter sit in shared memory.
+//    other 64 latent Q dims and the CTA's 32 rope dims sit in shared memory.
 //  * Warp roles per CTA (four warpgroups, registers moved by setmaxnreg):
 //    warps 0-3 stage each sequence's Q and, per page, read the CTA's partial S
 //    out of tensor memory, quantise it and send it to the peer; warp 4 issues
@@ -89,7 +89,7 @@ constexpr int kXSlots = 1;     // receive slots (peer partials)
 constexpr int kXData = kRowsPerTile * 128;     // 128 rows x 64 int16 (two 32-token halves)
 constexpr int kXSlot = kXData + 2 * kRowsPerTile * 4;  // + one fp32 scale per (row, half)
 constexpr int kXRowBytes = kXSlot / kRowsPerTile;      // one row's share: 136 bytes
-constexpr int kQRope = kRowsPerTile * 64;      // Q rope quarter: 128 rows x 32 bf16 (64B swizzle)
+constexpr int kQRope = kRowsPerTile * 64;      // the CTA's 32 Q rope dims: 128 rows x 32 bf16 (64B swizzle)
 constexpr int kQLat = kRowsPerTile * 128;      // Q latent dims [192, 256) of the CTA: 128 rows x 64 bf16
 
 constexpr int kOffK = 0;
@@ -455,7 +455,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
         }
       }
       // K pages need no Q: the loads run on across segment boundaries (a
-      // segment's Q rope quarter is loaded by the Q-staging warps).
+      // segment's Q rope dims are loaded by the Q-staging warps).
       int n = 0;
       while (w.valid && ok) {
         int phys = __ldg(P.block_table + static_cast<int64_t>(w.i) * P.max_blocks + w.p);
@@ -871,7 +871,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap q_rope, const __grid_const
     // that slot: they, not the softmax warps, do the quantisation and absorb
     // the SM-to-SM link's back-pressure.  A segment's Q is staged once the
     // previous segment's QKs are done (warp 0 also starts the TMA load of its
-    // rope quarter then), and before its first page can be sent.
+    // 32 rope dims then), and before its first page can be sent.
     const int quad = warp & 3;
     const int row = 32 * quad + static_cast<int>(lane);
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
