@@ -33,6 +33,10 @@ SMALL = [
     # of 96 with 48 heads): only those rows are exchanged between the CTAs
     ("partial_last_tile", 3, 3, 64, 1, [100, 300, 65], 640, True, None),
     ("h48_partial_last_tile", 2, 3, 48, 1, [200, 77], 576, True, 3),
+    # ~10 sequences per part: a segment boundary (Q staging, epilogue) every
+    # few pages, and more sequences than the scheduler block has threads
+    ("many_segments", 700, 1, 16, 1, "short", 640, False, None),
+    ("many_segments_128_heads", 300, 1, 128, 1, "short", 576, False, None),
 ]
 
 
