@@ -41,7 +41,8 @@
 //    partial while the softmax warps read theirs -> the peer's partial lands ->
 //    softmax -> P -> PV(n).  QK runs up to two pages ahead of the softmax (two
 //    S buffers, each handed back as soon as the softmax has read it); five K
-//    stages keep the HBM latency (about 1.3 us under load) covered.  Holding
+//    stages hide most of the HBM latency under load (with four the bench
+//    workload ran 5% slower; a sixth does not fit shared memory).  Holding
 //    QK back until PV(n-3) had been issued, or prefetching S a page early, was
 //    measured slower and dropped.
 //  * P is rounded to bf16 for the tensor cores.  On pages where one weight
@@ -78,7 +79,7 @@ constexpr uint32_t kRegsSoftmax = 168;
 // shares must fit in what the block was launched with (128 per thread).
 static_assert(128 * kRegsIssue + 128 * kRegsStage + 256 * kRegsSoftmax <= kThreads * 128u,
               "register split exceeds the launch allocation");
-// A K stage is held from its TMA issue (about 1.3 us of HBM latency under
+// A K stage is held from its TMA issue (microseconds of HBM latency under
 // load) until the PV of its page has read V, so the number of stages bounds the
 // pages in flight; five stages and a single exchange slot fill the 227 KB.
 constexpr int kStages = 5;
