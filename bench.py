@@ -42,14 +42,26 @@ L2_FLUSH_BYTES = 512 << 20
 BREAKDOWN_EVERY = 8  # every 8th timed pass also times each kernel on its own
 MIN_TIMED_S = 1.0    # the timed loop lasts at least this long, so that clock samples fall inside it
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one mla_decode_kernel launch,
-# taken from one ncu capture, keyed by a digest of the kernel's sources (comments
-# and whitespace ignored) and by the workload (name, entry stride).  A kernel
-# whose code changed since the capture reports null traffic.
-KERNEL_SOURCES = ("mla_decode.cu", "sm103_ptx.cuh", "mla_sched.cu", "mla_internal.h")
-MEASURED_TRAFFIC = {
-    ("de489b54d6bf90cb", "bench", 576): 626740224,
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the decode
+# kernel a workload runs on, taken from one ncu capture, keyed by a digest of
+# that kernel's sources (comments and whitespace ignored) and by the workload
+# (name, entry stride).  A kernel whose code changed since the capture reports
+# null traffic.  Tiles of at most 16 rows (s_q x heads per KV head) run on the
+# 16-row kernel, all others on the 128-row one.
+KERNEL_SOURCES = {
+    "mla_decode_kernel": ("mla_decode.cu", "mla_walk.cuh", "sm103_ptx.cuh", "mla_sched.cu", "mla_internal.h"),
+    "mla_decode_small_kernel": ("mla_decode_small.cu", "mla_walk.cuh", "sm103_ptx.cuh", "mla_sched.cu",
+                                "mla_internal.h"),
 }
+MEASURED_TRAFFIC = {
+    ("2a264c6594319436", "bench", 576): 626767872,
+    ("b8d1a09292498d35", "v2lite", 640): 53627648,
+}
+
+
+def decode_kernel(s_q: int, h_q: int, h_kv: int) -> str:
+    """Name of the decode kernel that runs this shape."""
+    return "mla_decode_small_kernel" if s_q * (h_q // h_kv) <= 16 else "mla_decode_kernel"
 
 
 def breakdown_steps(steps: int):
@@ -68,13 +80,13 @@ def passes_per_step(steps: int, seconds_per_pass: float, min_seconds: float = MI
     return max(1, int(np.ceil(need)))
 
 
-def kernel_digest() -> str:
-    """Hash of the decode kernel's sources with // comments and whitespace
+def kernel_digest(kernel: str = "mla_decode_kernel") -> str:
+    """Hash of a decode kernel's sources with // comments and whitespace
     removed: a comment edit keeps the measured traffic, a code edit drops it."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "mla_decode_attention_03_gb300", "csrc", name), encoding="utf-8") as f:
             code = re.sub(r"//[^\n]*", "", f.read())
         h.update("".join(code.split()).encode())
@@ -289,6 +301,7 @@ def run_ours(args, world, rank, local):
 
     hbm_peak, tf_peak, peak_src = peaks()
     achieved = nbytes / 1e9 / (ms_dec / 1e3)
+    kname = decode_kernel(w.s_q, w.h_q, w.h_kv)
     value = world * nbytes / 1e6 / ms_pass
     clocks = clk.summary()
     line = {
@@ -327,8 +340,8 @@ def run_ours(args, world, rank, local):
         "wall_s_timed_loop": round(wall, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": MEASURED_TRAFFIC.get((kernel_digest(), w.name, w.stride)),
-                     "kernel": "mla_decode_kernel", "peak_source": peak_src,
+                     "traffic": MEASURED_TRAFFIC.get((kernel_digest(kname), w.name, w.stride)),
+                     "kernel": kname, "peak_source": peak_src,
                      "tensor_tflops_achieved": round(flops / 1e9 / ms_dec, 1),
                      "tensor_frac": round(flops / 1e9 / ms_dec / tf_peak, 4)},
         "e2e": e2e,

@@ -70,9 +70,10 @@ typedef struct CUstream_st *mla_stream_t; /* the same type as cudaStream_t */
 const char *mla_status_string(mla_status_t status);
 
 /*
- * Recommended number of scheduler parts for `device`: how many 2-CTA decode
- * clusters fit on the GPU at once, divided among the (row tile, KV head)
- * grid dimensions of this shape.  Returns a count >= 1, or a negative
+ * Recommended number of scheduler parts for `device`: how many decode units
+ * fit on the GPU at once, divided among the (row tile, KV head) grid
+ * dimensions of this shape.  A unit is a 2-CTA cluster of the 128-row kernel,
+ * or, when s_q x (h_q / h_kv) <= 16, one CTA of the 16-row kernel.  Returns a count >= 1, or a negative
  * mla_status_t.  The first call per device queries occupancy; later calls are
  * cheap.
  */
@@ -92,7 +93,8 @@ size_t mla_workspace_bytes(int b, int s_q, int h_q, int num_parts);
  * Split-KV schedule (the role of FlashMLA's get_mla_metadata, called once per
  * decode step and shared by every layer).  Cuts the (sequence, page) order of
  * the batch into num_parts contiguous, cost-balanced parts; each part becomes
- * one 2-CTA cluster of the decode kernel.
+ * one decode unit per KV head (and row tile): a 2-CTA cluster of the 128-row
+ * kernel, or one CTA of the 16-row kernel.
  *   cache_seqlens  int32[b]            tokens per sequence (device)
  *   b              1 .. 16384
  *   num_parts      >= 1 (normally mla_num_parts())
@@ -173,12 +175,13 @@ mla_status_t mla_combine_splits(const int32_t *num_splits, int b, int s_q, int h
                                 mla_stream_t stream);
 
 /*
- * Diagnostic of the decode kernel's failure detection (no counterpart on the
+ * Diagnostic of the decode kernels' failure detection (no counterpart on the
  * pages).  Same arguments and host-side checks as mla_decode_with_kvcache, but
  * the kernel's TMA producer first waits on a barrier that nothing ever
- * completes, before it issues any copy.  Every wait in the kernel is bounded
+ * completes, before it issues any copy.  Every wait in the kernels is bounded
  * (about 2 s): that wait gives up, raises the CTA's abort flag, every other
- * warp role leaves its own wait, the CTAs free their tensor memory and exit,
+ * warp role leaves its own wait, the CTAs exit (the 128-row kernel's after
+ * freeing their tensor memory),
  * and MLA_ERR_TIMEOUT (-6) is written to *status.  out and lse are left
  * undefined.  The device stays usable: the next call decodes normally.  Lets a
  * caller check that a wait that can never end is reported, not hung on.
@@ -282,7 +285,7 @@ mla_status_t mla_decode_with_kvcache_static(const void *q, int b, int s_q, int h
  * their page counts, copies the inputs of run k to the device while run k-1
  * decodes, and copies the outputs of run k back while run k+1 decodes.  Each
  * run is an independent, complete decode (its own schedule over all
- * num_parts clusters), so the results equal those of mla_decode_with_kvcache
+ * num_parts parts), so the results equal those of mla_decode_with_kvcache
  * up to the rounding of a different split-KV cut (identical with chunks = 1).
  *
  * A pipeline object holds two CUDA streams (copies in, copies out) and the
@@ -331,7 +334,7 @@ size_t mla_host_scratch_bytes(int b, int s_q, int h_q, int max_blocks_per_seq, i
  * Arguments as for mla_decode_with_kvcache, except:
  *   q, block_table, cache_seqlens   HOST arrays (same shapes and types)
  *   out, lse                        HOST arrays, written
- *   num_parts                       clusters per run (normally mla_num_parts());
+ *   num_parts                       parts per run (normally mla_num_parts());
  *                                   there are no metadata/num_splits arguments:
  *                                   each run's schedule is made on the device
  *   chunks                          as for mla_host_chunks

@@ -15,8 +15,8 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libmla_decode.so"
-SOURCES = ["mla_decode.cu", "mla_sched.cu", "mla_cache.cu", "mla_api.cu", "mla_host.cu"]
-HEADERS = ["sm103_ptx.cuh", "mla_internal.h"]
+SOURCES = ["mla_decode.cu", "mla_decode_small.cu", "mla_sched.cu", "mla_cache.cu", "mla_api.cu", "mla_host.cu"]
+HEADERS = ["sm103_ptx.cuh", "mla_internal.h", "mla_walk.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -46,6 +46,12 @@ Shape tile_shape(int s_q, int h_q, int h_kv) {
   return s;
 }
 
+// Tiles of at most 16 rows (one query position x up to 16 heads per KV head,
+// or a few positions x fewer heads) run on the one-CTA kernel.
+bool small_tile(int s_q, int h_q, int h_kv) {
+  return static_cast<int64_t>(s_q) * (h_q / h_kv) <= mla::kSmallTileRows;
+}
+
 size_t workspace_o_bytes(int b, int s_q, int h_q, int num_parts) {
   const size_t slots = static_cast<size_t>(b) + static_cast<size_t>(num_parts);
   const size_t bytes = slots * static_cast<size_t>(s_q) * h_q * kDimV * 4;  // fp32 partials
@@ -86,27 +92,30 @@ int mla_num_parts(int s_q, int h_q, int h_kv, int device) {
   if (s_q < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
   if (h_q / h_kv > mla::kRowsPerTile) return MLA_ERR_UNSUPPORTED;
   static std::mutex mu;
-  static int cached[64];
+  static int cached[64][2];  // resident 2-CTA clusters of the 128-row kernel, CTAs of the 16-row kernel
   static bool have[64] = {false};
   if (device < 0 || device >= 64) return MLA_ERR_INVALID_ARG;
-  int clusters = 0;
+  const bool small = small_tile(s_q, h_q, h_kv);
+  int units = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!have[device]) {
       int prev = 0;
       if (cudaGetDevice(&prev) != cudaSuccess) return MLA_ERR_CUDA;
       if (cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
-      int c = 0;
+      int c = 0, k = 0;
       cudaError_t e = mla::decode_max_active_clusters(&c);
+      if (e == cudaSuccess) e = mla::decode_small_max_ctas(&k);
       cudaSetDevice(prev);
-      if (e != cudaSuccess || c < 1) return MLA_ERR_CUDA;
-      cached[device] = c;
+      if (e != cudaSuccess || c < 1 || k < 1) return MLA_ERR_CUDA;
+      cached[device][0] = c;
+      cached[device][1] = k;
       have[device] = true;
     }
-    clusters = cached[device];
+    units = cached[device][small ? 1 : 0];
   }
   const Shape s = tile_shape(s_q, h_q, h_kv);
-  int parts = clusters / (s.row_tiles * h_kv);
+  int parts = small ? units / h_kv : units / (s.row_tiles * h_kv);
   return parts < 1 ? 1 : parts;
 }
 
@@ -179,15 +188,20 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   if (chk != MLA_OK) return chk;
 
   const Shape s = tile_shape(s_q, h_q, h_kv);
+  const bool small = small_tile(s_q, h_q, h_kv);
   CUtensorMap q_rope, k_lat, k_rope;
   {
-    // the 32 rope dims of each CTA's Q columns; its latent dims are read by the kernel's threads
+    // 128-row kernel: the 32 rope dims of each CTA's Q columns (its latent
+    // dims are read by the kernel's threads).  16-row kernel: a 64-dim slice
+    // of all of a tile's rows, the same 128B swizzle as the cache pages.
     const cuuint64_t row = static_cast<cuuint64_t>(kDimQK) * 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(h_q),
                           static_cast<cuuint64_t>(s_q), static_cast<cuuint64_t>(b)};
     cuuint64_t strides[3] = {row, row * h_q, row * h_q * s_q};
-    cuuint32_t box[4] = {32, static_cast<cuuint32_t>(s.heads_per_kv), static_cast<cuuint32_t>(s.q_per_tile), 1};
-    mla_status_t r = encode(&q_rope, 4, const_cast<void*>(q), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    cuuint32_t box[4] = {small ? 64u : 32u, static_cast<cuuint32_t>(s.heads_per_kv),
+                         static_cast<cuuint32_t>(s.q_per_tile), 1};
+    mla_status_t r = encode(&q_rope, 4, const_cast<void*>(q), dims, strides, box,
+                            small ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (r != MLA_OK) return r;
   }
   {
@@ -231,8 +245,9 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   p.stall_test = stall_test ? 1 : 0;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (mla::launch_decode(p, q_rope, k_lat, k_rope, num_parts, s.row_tiles, st) != cudaSuccess)
-    return MLA_ERR_CUDA;
+  const cudaError_t e = small ? mla::launch_decode_small(p, q_rope, k_lat, num_parts, st)
+                       : mla::launch_decode(p, q_rope, k_lat, k_rope, num_parts, s.row_tiles, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (!with_combine) return MLA_OK;
   return mla_combine_splits(num_splits, b, s_q, h_q, workspace, num_parts, out, lse, stream);
 }

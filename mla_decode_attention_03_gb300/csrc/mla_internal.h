@@ -11,9 +11,10 @@ constexpr int kDimQK = 576;     // latent 512 + rope 64
 constexpr int kDimV = 512;      // value = leading 512 latent dims
 constexpr int kPage = 64;       // tokens per cache page
 constexpr int kRowsPerTile = 128;
+constexpr int kSmallTileRows = 16;  // tiles of at most this many rows take the one-CTA kernel
 constexpr int kMetaInts = 8;    // ints per scheduler part
 constexpr int kSegmentCost = 6; // fixed scheduler cost of one (sequence, part) segment, in pages (measured: 2, 4, 6, 8, 12 -> 6 best)
-constexpr int kMinPartCost = 10;  // smallest part, in cost units (independent of kSegmentCost)
+constexpr int kMinPartCost = 4;   // smallest part, in cost units (independent of kSegmentCost)
 constexpr int kMaxMetadataBatch = 16384;  // sequences the scheduler stages in shared memory
 
 // Device-side status codes (written to the caller's status word).
@@ -62,6 +63,11 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, int32_t* metadata,
                             int32_t* num_splits, int32_t* status, cudaStream_t stream);
 cudaError_t decode_max_active_clusters(int* clusters);
+// One CTA per (part, KV head) for shapes with s_q * heads_per_kv <= kSmallTileRows.
+int decode_small_smem_bytes();
+cudaError_t launch_decode_small(const DecodeParams& p, const CUtensorMap& q_full, const CUtensorMap& k_lat, int num_parts,
+                                cudaStream_t stream);
+cudaError_t decode_small_max_ctas(int* ctas);
 cudaError_t launch_write_cache(const void* kv_c, int64_t kv_c_row_elems, const void* k_pe, int64_t k_pe_row_elems,
                                const int64_t* slot_mapping, int64_t num_tokens, void* kcache, int64_t num_slots,
                                int stride, int32_t* status, cudaStream_t stream);

@@ -1,11 +1,13 @@
-"""Failure detection of the decode kernel on the GPU, without a GPU fault.
+"""Failure detection of the decode kernels on the GPU, without a GPU fault.
 
-Every wait in the decode kernel is bounded (about 2 s).  The diagnostic entry
+Every wait in the decode kernels is bounded (about 2 s).  The diagnostic entry
 point mla_selftest_wait_timeout runs the decode with one wait on a barrier
 that nothing ever completes, placed before any copy is issued: the wait gives
-up, every warp role of both CTAs of each cluster leaves its own wait through
-the CTA's abort flag, and the status word reports MLA_ERR_TIMEOUT (-6).  The
-context must stay usable: a normal decode right after it matches the oracle.
+up, every other warp role leaves its own wait through the CTA's abort flag
+(both CTAs of each cluster in the 128-row kernel), and the status word reports
+MLA_ERR_TIMEOUT (-6).  The context must stay usable: a normal decode right
+after it matches the oracle.  Both kernels are covered: 128 heads per KV head
+run on the 128-row kernel, 16 on the 16-row one.
 """
 import pytest
 import torch
@@ -17,19 +19,20 @@ from tests._gpu_helpers import all_rows, assert_matches, run_gpu, to_device
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_that_never_ends_reports_timeout_and_context_survives():
-    w = W.make(2, 1, 128, 1, [100, 300], stride=640, seed=28)
+@pytest.mark.parametrize("h_q", [128, 16])
+def test_wait_that_never_ends_reports_timeout_and_context_survives(h_q):
+    w = W.make(2, 1, h_q, 1, [100, 300], stride=640, seed=28)
     dev = to_device(w)
     status = ops.new_status()
     parts = 4
     meta, nsplit = ops.get_mla_metadata(dev["cache_seqlens"], parts, status)
-    out = torch.empty((w.b, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((w.b, 128, 1), dtype=torch.float32, device="cuda")
-    ws = torch.empty((ops.workspace_bytes(w.b, 1, 128, parts),), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.b, 1, h_q, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.b, h_q, 1), dtype=torch.float32, device="cuda")
+    ws = torch.empty((ops.workspace_bytes(w.b, 1, h_q, parts),), dtype=torch.uint8, device="cuda")
     kc = dev["kcache"]
     bt, sl = dev["block_table"], dev["cache_seqlens"]
     rc = ops.load_library().mla_selftest_wait_timeout(
-        dev["q"].data_ptr(), w.b, 1, 128, 576, kc.data_ptr(), w.num_blocks, 64, 1, ops.entry_stride(kc),
+        dev["q"].data_ptr(), w.b, 1, h_q, 576, kc.data_ptr(), w.num_blocks, 64, 1, ops.entry_stride(kc),
         bt.data_ptr(), bt.shape[1], sl.data_ptr(), 512, meta.data_ptr(), parts, nsplit.data_ptr(),
         w.softmax_scale, 0, out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), status.data_ptr(),
         torch.cuda.current_stream().cuda_stream)
@@ -43,12 +46,11 @@ def test_wait_that_never_ends_reports_timeout_and_context_survives():
 
 @pytest.mark.parametrize("name", ["v2lite", "tiny"])
 def test_small_head_tiles_repeated_back_to_back(name):
-    """Tiles with fewer live rows than 128 (16 heads) exchange only their live
-    rows, and the sender warps without a live row skip the slot credit.  A
-    waiter that could fall two phases behind the credit would show up only
-    after several back-to-back decodes (a timeout, not a fault): 40 of them,
-    with the status word checked after every one and the last output compared
-    with the oracle on every row."""
+    """16-head tiles on the 16-row kernel, many back-to-back decodes: a waiter
+    on one of its two-slot barriers (stages, Q buffers, maxima, P buffers)
+    that could fall two phases behind would show up only after several of
+    them (a timeout, not a fault): 40 decodes, the status word checked every
+    eighth, the last output compared with the oracle on every row."""
     w = W.named(name)
     dev = to_device(w)
     parts = ops.num_parts(w.s_q, w.h_q, w.h_kv)

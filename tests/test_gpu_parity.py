@@ -37,6 +37,13 @@ SMALL = [
     # few pages, and more sequences than the scheduler block has threads
     ("many_segments", 700, 1, 16, 1, "short", 640, False, None),
     ("many_segments_128_heads", 300, 1, 128, 1, "short", 576, False, None),
+    # tiles of at most 16 rows (the 16-row kernel): query positions x heads
+    # per KV head = 16, 12 and 4 rows; causal rows with nothing visible
+    # (L=1, 2 with several positions); split sequences; four KV heads
+    ("rows16_causal_two_positions", 3, 2, 8, 1, [1, 2, 333], 640, True, None),
+    ("rows16_causal_four_positions_split", 3, 4, 4, 1, [65, 130, 7], 576, True, 3),
+    ("rows12_causal_three_positions", 2, 3, 4, 1, [200, 64], 640, True, None),
+    ("rows4_four_kv_heads_split", 2, 1, 16, 4, [150, 90], 576, False, 2),
 ]
 
 

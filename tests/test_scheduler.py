@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-SEGMENT_COST, MIN_PART_COST, PAGE = 6, 10, 64
+SEGMENT_COST, MIN_PART_COST, PAGE = 6, 4, 64
 
 
 def pages_of(L):
