@@ -387,6 +387,8 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
     for (int b = 0; b < 2; ++b)
 #pragma unroll
       for (int j = 0; j < 8; ++j) o[b][j][0] = o[b][j][1] = o[b][j][2] = o[b][j][3] = 0.f;
+    int seg_nsplit = 1;
+    int64_t seg_oslot = 0;
 
     while (ok && w.valid) {
       const int pb = n & 1;
@@ -409,6 +411,9 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
       }
 
       if (w.first()) {
+        // where this segment's rows go: read now, used at its end
+        seg_nsplit = __ldg(P.num_splits + w.i + 1) - __ldg(P.num_splits + w.i);
+        seg_oslot = static_cast<int64_t>(__ldg(P.num_splits + w.i)) + w.k;
 #pragma unroll
         for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -460,8 +465,8 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
       // ---- epilogue at the end of a segment: normalised rows, bf16 to out when
       // the sequence has one segment, else fp32 to its split slot
       if (last) {
-        const int nsplit = __ldg(P.num_splits + w.i + 1) - __ldg(P.num_splits + w.i);
-        const int64_t oslot = static_cast<int64_t>(__ldg(P.num_splits + w.i)) + w.k;
+        const int nsplit = seg_nsplit;
+        const int64_t oslot = seg_oslot;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (!row_ok[u]) continue;
