@@ -190,22 +190,34 @@ mla_status_t decode_impl(const void* q, int b, int s_q, int h_q, int d, const vo
   const Shape s = tile_shape(s_q, h_q, h_kv);
   const bool small = small_tile(s_q, h_q, h_kv);
   CUtensorMap q_rope, k_lat, k_rope;
-  {
-    // 128-row kernel: the 32 rope dims of each CTA's Q columns (its latent
-    // dims are read by the kernel's threads).  16-row kernel: a 64-dim slice
-    // of all of a tile's rows, the same 128B swizzle as the cache pages.
-    const cuuint64_t row = static_cast<cuuint64_t>(kDimQK) * 2;
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(h_q),
-                          static_cast<cuuint64_t>(s_q), static_cast<cuuint64_t>(b)};
-    cuuint64_t strides[3] = {row, row * h_q, row * h_q * s_q};
-    cuuint32_t box[4] = {small ? 64u : 32u, static_cast<cuuint32_t>(s.heads_per_kv),
-                         static_cast<cuuint32_t>(s.q_per_tile), 1};
-    mla_status_t r = encode(&q_rope, 4, const_cast<void*>(q), dims, strides, box,
-                            small ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  const cuuint64_t qrow = static_cast<cuuint64_t>(kDimQK) * 2;
+  const cuuint64_t entry = static_cast<cuuint64_t>(stride) * 2;
+  if (small) {
+    // 16-row kernel: views whose two innermost dimensions are (64 dims, 9
+    // slices of 64), so that one copy moves a segment's Q (all its rows) or
+    // a page (all 64 tokens) as 128-byte (row, slice) rows, 128B swizzle
+    cuuint64_t qdims[5] = {64, kDimQK / 64, static_cast<cuuint64_t>(h_q), static_cast<cuuint64_t>(s_q),
+                           static_cast<cuuint64_t>(b)};
+    cuuint64_t qstrides[4] = {128, qrow, qrow * h_q, qrow * h_q * s_q};
+    cuuint32_t qbox[5] = {64, kDimQK / 64, static_cast<cuuint32_t>(s.heads_per_kv),
+                          static_cast<cuuint32_t>(s_q), 1};
+    mla_status_t r = encode(&q_rope, 5, const_cast<void*>(q), qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != MLA_OK) return r;
-  }
-  {
-    const cuuint64_t entry = static_cast<cuuint64_t>(stride) * 2;
+    cuuint64_t kdims[4] = {64, kDimQK / 64, static_cast<cuuint64_t>(h_kv), static_cast<cuuint64_t>(num_blocks) * kPage};
+    cuuint64_t kstrides[3] = {128, entry, entry * h_kv};
+    cuuint32_t kbox[4] = {64, kDimQK / 64, 1, static_cast<cuuint32_t>(kPage)};
+    r = encode(&k_lat, 4, const_cast<void*>(kcache), kdims, kstrides, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != MLA_OK) return r;
+  } else {
+    {
+      // the 32 rope dims of each CTA's Q columns; its latent dims are read by the kernel's threads
+      cuuint64_t dims[4] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(h_q),
+                            static_cast<cuuint64_t>(s_q), static_cast<cuuint64_t>(b)};
+      cuuint64_t strides[3] = {qrow, qrow * h_q, qrow * h_q * s_q};
+      cuuint32_t box[4] = {32, static_cast<cuuint32_t>(s.heads_per_kv), static_cast<cuuint32_t>(s.q_per_tile), 1};
+      mla_status_t r = encode(&q_rope, 4, const_cast<void*>(q), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+      if (r != MLA_OK) return r;
+    }
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(h_kv),
                           static_cast<cuuint64_t>(num_blocks) * kPage};
     cuuint64_t strides[2] = {entry, entry * h_kv};

@@ -10,8 +10,11 @@
 // warp-level tensor-core instructions (m16n8k16, bf16 in, fp32 accumulate),
 // operands from shared memory through ldmatrix:
 //  * the producer warp loads a segment's Q (16 rows x 576 dims, two buffers)
-//    and then its pages, all 576 dims of a page as nine 64-dim boxes (128B
-//    swizzle) into one of two stages (73,728 B each); every page is read once;
+//    and then its pages, all 576 dims of a page into one of two stages
+//    (73,728 B each), each with one TMA copy through a view of the cache whose
+//    two innermost dimensions are (64 dims, 9 slices of 64): a stage holds
+//    128-byte rows (token, slice) with the 128B swizzle; every page is read
+//    once;
 //  * four score warps take 16 tokens each: S = Q K^T, the row maxima swapped
 //    through shared memory, P = exp(scale (S - m)) as bf16 together with its
 //    bf16 rounding error (so P carries ~16 bits), written in the A-fragment
@@ -34,11 +37,9 @@ constexpr int kSmWarps = kSmScoreWarps + kSmOutWarps;
 constexpr int kSmThreads = 32 * (kSmWarps + 1);   // + one TMA producer warp (8)
 constexpr int kSmRows = 16;
 constexpr int kSmStages = 2;
-constexpr int kSmBox = kPage * 128;               // 64 tokens x 64 dims bf16, 128B swizzle: 8192 B
-constexpr int kSmBoxes = kDimQK / 64;             // 9
-constexpr int kSmStage = kSmBoxes * kSmBox;       // 73728 B: all 576 dims of a page
-constexpr int kSmQBox = kSmRows * 128;            // 16 rows x 64 dims: 2048 B
-constexpr int kSmQBuf = kSmBoxes * kSmQBox;       // 18432 B
+constexpr int kSmBoxes = kDimQK / 64;             // 9 slices of 64 dims (128 B) per token or Q row
+constexpr int kSmStage = kPage * kSmBoxes * 128;  // 73728 B: all 576 dims of a page
+constexpr int kSmQBuf = kSmRows * kSmBoxes * 128; // 18432 B
 // P buffer: hi and lo fragments [chunk of 16 tokens][lane][4 registers] (u32),
 // the rescale factor per row, and at a segment's end the score warps' partial
 // row sums and the row maxima.
@@ -68,14 +69,35 @@ constexpr int kSmBarStall = 14;
 constexpr int kSmNumBars = 15;
 constexpr int kSmOffMisc = kSmOffBar + kSmNumBars * 8;
 constexpr int kSmSmemBytes = kSmOffMisc + 16 + 1024;  // abort flag; slack to align the base to 1024 B
-static_assert(kSmOffQ % 1024 == 0 && kSmQBuf % 1024 == 0, "Q boxes must sit on 128B-swizzle atoms");
+static_assert(kSmOffQ % 1024 == 0 && kSmQBuf % 1024 == 0 && kSmStage % 1024 == 0,
+              "TMA destinations must sit on 128B-swizzle atoms");
 static_assert(kSmOffP % 16 == 0 && kSmPBuf % 16 == 0 && kSmOffBar % 8 == 0, "alignment");
 static_assert(kSmSmemBytes <= 232448, "shared memory per CTA");
 
-// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-row
-// box with the 128B swizzle TMA writes (chunk index XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128(uint32_t box, int row, int chunk) {
-  return box + static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+// Address of 16-byte chunk `chunk` (0..7) of 128-byte row `row` of a region
+// that TMA filled with the 128B swizzle from a 1024-byte aligned base (the
+// chunk index is XORed with the row index mod 8).  Rows are (token, slice)
+// or (Q row, slice) pairs: row = 9 * token + slice.
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int chunk) {
+  return base + static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, uint32_t bar, int c0, int c1, int c2,
+                                            int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -160,6 +182,12 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
       tma_prefetch_desc(&k_map);
       const uint64_t evict_first = l2_policy_evict_first();
       const uint32_t q_bytes = static_cast<uint32_t>(kSmBoxes * 128 * rows_live);
+      // The part's first page id, read alongside the walk's own start (a
+      // part never starts in an empty sequence), not after it.
+      const int i0 = __ldg(meta + 0), p0 = __ldg(meta + 1);
+      int phys0 = -1;
+      if (i0 >= 0 && i0 < P.b && p0 >= 0 && p0 < P.max_blocks)
+        phys0 = __ldg(P.block_table + static_cast<int64_t>(i0) * P.max_blocks + p0);
       PageWalk w;
       w.start(meta, P.cache_seqlens, P.max_blocks);
       int n = 0, seg = 0;
@@ -171,13 +199,13 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
           ok = mbar_wait(bar(kSmBarQEmpty + qb), ((seg >> 1) & 1) ^ 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(kSmBarQFull + qb), q_bytes);
-          const uint32_t qdst = base + kSmOffQ + qb * kSmQBuf;
-#pragma unroll 1
-          for (int t = 0; t < kSmBoxes; ++t)
-            tma_load_4d(qdst + t * kSmQBox, &q_map, bar(kSmBarQFull + qb), 64 * t, g * hpk, 0, w.i);
+          // rows (Q row, slice) = the box {64 dims, 9 slices, hpk heads, s_q positions}
+          tma_load_5d(base + kSmOffQ + qb * kSmQBuf, &q_map, bar(kSmBarQFull + qb), 0, 0, g * hpk, 0, w.i);
           ++seg;
         }
-        int phys = __ldg(P.block_table + static_cast<int64_t>(w.i) * P.max_blocks + w.p);
+        int phys = (n == 0 && w.i == i0 && w.p == p0)
+                       ? phys0
+                       : __ldg(P.block_table + static_cast<int64_t>(w.i) * P.max_blocks + w.p);
         if (phys < 0 || phys >= P.num_blocks) {
           raise_status(P.status, kStatusBadBlockId);
           phys = 0;
@@ -186,10 +214,9 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
         ok = mbar_wait(bar(kSmBarEmpty + st), ((n / kSmStages) & 1) ^ 1, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(kSmBarFull + st), kSmStage);
-        const uint32_t dst = base + kSmOffK + st * kSmStage;
-#pragma unroll 1
-        for (int t = 0; t < kSmBoxes; ++t)
-          tma_load_3d_hint(dst + t * kSmBox, &k_map, bar(kSmBarFull + st), 64 * t, g, phys * kPage, evict_first);
+        // rows (token, slice) = the box {64 dims, 9 slices, 1 KV head, 64 tokens}
+        tma_load_4d_hint(base + kSmOffK + st * kSmStage, &k_map, bar(kSmBarFull + st), 0, 0, g, phys * kPage,
+                         evict_first);
         ++n;
         w.advance();
       }
@@ -249,8 +276,8 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
       const uint32_t kst = base + kSmOffK + st * kSmStage;
 
       // ---- S = Q K^T for this warp's 16 tokens (two 8-token tiles j) over
-      // the 576 dims, per 64-dim box two pairs of k-steps; one accumulator per
-      // tile and k-step parity keeps the dependent chains short
+      // the 576 dims, per 64-dim slice two pairs of k-steps; one accumulator
+      // per tile and k-step parity keeps the dependent chains short
       float acc[2][2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -260,18 +287,16 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
         const int ar = lane & 15, ac = lane >> 4;
         const int bt = 16 * sw + (lane & 7), bc = lane >> 3;
 #pragma unroll
-        for (int box = 0; box < kSmBoxes; ++box) {
-          const uint32_t qbox = q_base + box * kSmQBox;
-          const uint32_t kbox = kst + box * kSmBox;
+        for (int sl = 0; sl < kSmBoxes; ++sl) {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t a0[4], a1[4];
-            ldsm_x4(sw128(qbox, ar, 4 * h2 + ac), a0[0], a0[1], a0[2], a0[3]);
-            ldsm_x4(sw128(qbox, ar, 4 * h2 + 2 + ac), a1[0], a1[1], a1[2], a1[3]);
+            ldsm_x4(sw128(q_base, kSmBoxes * ar + sl, 4 * h2 + ac), a0[0], a0[1], a0[2], a0[3]);
+            ldsm_x4(sw128(q_base, kSmBoxes * ar + sl, 4 * h2 + 2 + ac), a1[0], a1[1], a1[2], a1[3]);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               uint32_t b0, b1, b2, b3;
-              ldsm_x4(sw128(kbox, bt + 8 * j, 4 * h2 + bc), b0, b1, b2, b3);
+              ldsm_x4(sw128(kst, kSmBoxes * (bt + 8 * j) + sl, 4 * h2 + bc), b0, b1, b2, b3);
               mma16816(acc[j][0], a0[0], a0[1], a0[2], a0[3], b0, b1);
               mma16816(acc[j][1], a1[0], a1[1], a1[2], a1[3], b2, b3);
             }
@@ -368,7 +393,7 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
     }
   } else {
     // ================================================= output warps
-    // Warp ov takes output columns 128 ov .. 128 ov + 127: latent boxes 2 ov
+    // Warp ov takes output columns 128 ov .. 128 ov + 127: latent slices 2 ov
     // and 2 ov + 1 of each page, one page behind the score warps.
     const int ov = warp - kSmScoreWarps;
     const int rows_total = P.s_q * P.h_q;
@@ -444,11 +469,11 @@ mla_decode_small_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_
         const uint4 pl = *reinterpret_cast<const uint4*>(pbuf + kSmPLo + (kc * 32 + lane) * 16);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-          const uint32_t vbox = kst + (2 * ov + b) * kSmBox;
 #pragma unroll
           for (int jp = 0; jp < 4; ++jp) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sw128(vbox, 16 * kc + (lane & 15), 2 * jp + (lane >> 4)), b0, b1, b2, b3);
+            ldsm_x4_t(sw128(kst, kSmBoxes * (16 * kc + (lane & 15)) + 2 * ov + b, 2 * jp + (lane >> 4)), b0, b1,
+                      b2, b3);
             mma16816(o[b][2 * jp], ph.x, ph.y, ph.z, ph.w, b0, b1);
             mma16816(o[b][2 * jp + 1], ph.x, ph.y, ph.z, ph.w, b2, b3);
             mma16816(o[b][2 * jp], pl.x, pl.y, pl.z, pl.w, b0, b1);
