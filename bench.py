@@ -55,7 +55,7 @@ KERNEL_SOURCES = {
 }
 MEASURED_TRAFFIC = {
     ("2a264c6594319436", "bench", 576): 626767872,
-    ("f0b2bc0efdd5a034", "v2lite", 640): 53629952,
+    ("eb6770506d7dc930", "v2lite", 640): 53668608,
 }
 
 
