@@ -72,16 +72,22 @@ def test_named_full_size_all_rows(name, stride):
     assert_matches(w, out, lse, all_rows(w))
 
 
-def test_lazy_rescale_every_page():
+# Behaviour tests run on both kernels: 128 heads per KV head (the 128-row
+# cluster kernel) and 16 (the 16-row kernel; 8 heads when s_q = 2).
+KERNEL_HEADS = [128, 16]
+
+
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_lazy_rescale_every_page(h_q):
     """The running max is moved (and O and the row sums rescaled) only when it
-    grows by more than 8 log2 units.  Here one key per page climbs by about 9.6
+    grows by more than 8 log2 units (the 16-row kernel rescales on every page).  Here one key per page climbs by about 9.6
     log2 units over the previous page's (q has 4 in dim 0 for every head, the
     climbing key 40*(p+1) there), so the rescale runs on nearly every page of
     every row, while the other keys of earlier pages still carry weight that a
     wrong rescale factor would distort by 2^9.  Sequences are cut into several
     pieces so the merge of rescaled pieces is covered too."""
     lens = [6 * 64, 5 * 64 - 17, 7 * 64 + 3, 64]
-    w = W.make(len(lens), 1, 128, 1, lens, stride=640, seed=27)
+    w = W.make(len(lens), 1, h_q, 1, lens, stride=640, seed=27)
     w.q[..., 0] = 4.0
     bt = w.block_table.numpy()
     for i, L in enumerate(lens):
@@ -93,11 +99,12 @@ def test_lazy_rescale_every_page():
         assert_matches(w, out, lse, all_rows(w))
 
 
-def test_negative_length_reported_and_treated_as_empty():
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_negative_length_reported_and_treated_as_empty(h_q):
     """A negative cache_seqlens entry is outside the contract; the scheduler
     reports MLA_ERR_BAD_SEQLEN in the status word, the decode treats that
     sequence as empty (no page of it is read), and the context stays usable."""
-    w = W.make(3, 1, 128, 1, [200, 64, 300], seed=26)
+    w = W.make(3, 1, h_q, 1, [200, 64, 300], seed=26)
     dev = to_device(w)
     sl = dev["cache_seqlens"].clone()
     sl[1] = -5
@@ -116,8 +123,9 @@ def test_negative_length_reported_and_treated_as_empty():
     assert_matches(w_ok, out, lse, all_rows(w_ok))
 
 
-def test_stride_576_and_640_identical():
-    w640 = W.make(6, 1, 128, 1, [700, 64, 1, 129, 1000, 333], stride=640, seed=21, poison=True)
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_stride_576_and_640_identical(h_q):
+    w640 = W.make(6, 1, h_q, 1, [700, 64, 1, 129, 1000, 333], stride=640, seed=21, poison=True)
     w576 = W.Workload(**{**w640.__dict__, "kcache_alloc": w640.kcache_alloc[..., :576].contiguous(),
                          "stride": 576})
     o1, l1, _, _ = run_gpu(w640, parts=5)
@@ -125,25 +133,28 @@ def test_stride_576_and_640_identical():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
 @pytest.mark.parametrize("causal,s_q", [(False, 1), (True, 2)])
-def test_repeated_runs_bitwise_identical(causal, s_q):
+def test_repeated_runs_bitwise_identical(causal, s_q, h_q):
     """Many short segments (1- and 2-page sequences, parts that cut sequences)
     stress every hand-off between the kernel's warp roles; any race shows up as
     a run that differs from the first one."""
     lens = [700, 64, 3000, 1, 129, 4096, 65, 128, 2, 900]
-    w = W.make(len(lens), s_q, 128, 1, lens, causal=causal, stride=640, seed=23)
+    heads = h_q if h_q == 128 else 16 // s_q
+    w = W.make(len(lens), s_q, heads, 1, lens, causal=causal, stride=640, seed=23)
     first = run_gpu(w, parts=11)[:2]
     for _ in range(12):
         o, l = run_gpu(w, parts=11)[:2]
         assert torch.equal(o, first[0]) and torch.equal(l, first[1])
 
 
-def test_many_reruns_bitwise_identical():
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_many_reruns_bitwise_identical(h_q):
     """A race between warp roles of the two CTAs of a cluster (an exchange slot
     returned to the peer before every load of it was ordered) showed up in
     about one run in 300 of this short-segment, poisoned-padding workload; 400
     back-to-back runs on the same inputs must all equal the first."""
-    w = W.make(6, 1, 128, 1, [700, 64, 1, 129, 1000, 333], stride=640, seed=21, poison=True)
+    w = W.make(6, 1, h_q, 1, [700, 64, 1, 129, 1000, 333], stride=640, seed=21, poison=True)
     dev = to_device(w)
     status = ops.new_status()
     meta, nsplit = ops.get_mla_metadata(dev["cache_seqlens"], 5, status)
@@ -159,8 +170,9 @@ def test_many_reruns_bitwise_identical():
     assert differ == 0
 
 
-def test_page_permutation_identical():
-    w = W.make(4, 2, 128, 1, [300, 129, 64, 1000], causal=True, seed=22, permute=False)
+@pytest.mark.parametrize("h_q", [128, 8])
+def test_page_permutation_identical(h_q):
+    w = W.make(4, 2, h_q, 1, [300, 129, 64, 1000], causal=True, seed=22, permute=False)
     o1, l1, _, _ = run_gpu(w, parts=4)
     perm = torch.from_numpy(np.random.default_rng(5).permutation(w.num_blocks))
     kc2 = torch.empty_like(w.kcache_alloc)
@@ -172,15 +184,17 @@ def test_page_permutation_identical():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
 @pytest.mark.parametrize("parts", [1, 2, 9, 150])
-def test_split_count_invariance(parts):
-    w = W.make(3, 1, 128, 1, [2000, 513, 4096], stride=640, seed=23)
+def test_split_count_invariance(parts, h_q):
+    w = W.make(3, 1, h_q, 1, [2000, 513, 4096], stride=640, seed=23)
     out, lse, meta, nsplit = run_gpu(w, parts=parts)
     assert_matches(w, out, lse, all_rows(w))
 
 
-def test_bad_block_id_reported_not_faulted():
-    w = W.make(2, 1, 128, 1, [200, 100], seed=24)
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_bad_block_id_reported_not_faulted(h_q):
+    w = W.make(2, 1, h_q, 1, [200, 100], seed=24)
     w.block_table[1, 0] = w.num_blocks + 5  # outside the cache
     dev = to_device(w)
     status = ops.new_status()
