@@ -22,22 +22,23 @@ pytestmark = pytest.mark.gpu
 LAYERS = 3
 
 
-def _layer_inputs(seed, stride=640):
+def _layer_inputs(seed, stride=640, h_q=128):
     # same lengths and block table for every layer (one step: pages in order,
     # so every layer's table is the same), different q and cache
-    return W.make(6, 1, 128, 1, [700, 64, 3000, 1, 129, 4096], stride=stride, seed=seed, permute=False)
+    return W.make(6, 1, h_q, 1, [700, 64, 3000, 1, 129, 4096], stride=stride, seed=seed, permute=False)
 
 
-def test_captured_step_equals_eager_and_tracks_new_inputs():
-    ws = [_layer_inputs(40 + k) for k in range(LAYERS)]
+@pytest.mark.parametrize("h_q", [128, 16])
+def test_captured_step_equals_eager_and_tracks_new_inputs(h_q):
+    ws = [_layer_inputs(40 + k, h_q=h_q) for k in range(LAYERS)]
     assert all(torch.equal(w.block_table, ws[0].block_table) for w in ws)
     sl = ws[0].cache_seqlens.cuda()
     bt = ws[0].block_table.cuda()
     qs = [w.q.cuda() for w in ws]
     kcs = [w.kcache_alloc.cuda()[..., :576] for w in ws]
-    dec = ops.MLADecoder(6, 1, 128, 1, parts=11)
-    outs = [torch.empty((6, 1, 128, 512), dtype=torch.bfloat16, device="cuda") for _ in range(LAYERS)]
-    lses = [torch.empty((6, 128, 1), dtype=torch.float32, device="cuda") for _ in range(LAYERS)]
+    dec = ops.MLADecoder(6, 1, h_q, 1, parts=11)
+    outs = [torch.empty((6, 1, h_q, 512), dtype=torch.bfloat16, device="cuda") for _ in range(LAYERS)]
+    lses = [torch.empty((6, h_q, 1), dtype=torch.float32, device="cuda") for _ in range(LAYERS)]
     scale = ws[0].softmax_scale
 
     def step():
@@ -70,7 +71,7 @@ def test_captured_step_equals_eager_and_tracks_new_inputs():
 
     # new q values in place: the replay must follow them
     for k in range(LAYERS):
-        qs[k].copy_(W.make(6, 1, 128, 1, [1] * 6, seed=90 + k).q.cuda())
+        qs[k].copy_(W.make(6, 1, h_q, 1, [1] * 6, seed=90 + k).q.cuda())
     graph.replay()
     torch.cuda.synchronize()
     got = [(o.clone(), l.clone()) for o, l in zip(outs, lses)]

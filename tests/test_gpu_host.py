@@ -38,9 +38,10 @@ def test_one_run_equals_device_call():
     assert torch.equal(o_h, o_dev.cpu()) and torch.equal(l_h, l_dev.cpu())
 
 
+@pytest.mark.parametrize("h_q", [128, 8])
 @pytest.mark.parametrize("chunks", [2, 3, 8])
-def test_several_runs_all_rows(chunks):
-    w = W.make(9, 2, 128, 1, [0, 5, 64, 129, 700, 1, 3000, 0, 333], stride=640, causal=True, seed=32,
+def test_several_runs_all_rows(chunks, h_q):
+    w = W.make(9, 2, h_q, 1, [0, 5, 64, 129, 700, 1, 3000, 0, 333], stride=640, causal=True, seed=32,
                poison=True)
     dev = to_device(w)
     hd = ops.HostDecoder(w.b, w.s_q, w.h_q, w.block_table.shape[1], w.h_kv, parts=5)

@@ -58,6 +58,8 @@ def test_static_scratch_matches_caller_workspace_on_two_calls():
         (W.make(6, 1, 128, 1, [300, 4096, 1, 64, 2000, 700], stride=640, seed=31), 9),
         # causal s_q = 2 (two row tiles), a different split pattern
         (W.make(5, 2, 128, 1, [129, 2, 3000, 64, 900], stride=576, causal=True, seed=32), 7),
+        # 16 heads: the 16-row kernel
+        (W.make(6, 1, 16, 1, [300, 4096, 1, 64, 2000, 700], stride=640, seed=33), 9),
     ]
     for w, parts in cases:
         d = _inputs(w, parts)
