@@ -215,3 +215,16 @@ def test_metadata_covers_every_page_once():
     for parts in (1, 7, 76, 200):
         meta, nsplit = ops.get_mla_metadata(torch.from_numpy(sl).cuda(), parts)
         check_schedule(sl, parts, meta.cpu().numpy(), nsplit.cpu().numpy())
+
+
+def test_num_parts_follows_the_kernel():
+    """Tiles of at most 16 rows run one CTA per part and KV head (one per SM),
+    larger tiles one 2-CTA cluster per part, row tile and KV head."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    small = ops.num_parts(1, 16, 1)
+    big = ops.num_parts(1, 128, 1)
+    assert small == sms and big == sms // 2
+    assert ops.num_parts(1, 16, 2) == sms // 2        # 8 heads per KV head, 2 KV heads
+    assert ops.num_parts(2, 8, 1) == sms              # 2 positions x 8 heads = 16 rows
+    assert ops.num_parts(2, 128, 1) == big // 2       # two 128-row tiles
+    assert ops.num_parts(1, 32, 1) == big             # 32 rows: the cluster kernel
