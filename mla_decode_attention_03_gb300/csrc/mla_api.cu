@@ -354,6 +354,7 @@ mla_status_t mla_combine_splits(const int32_t* num_splits, int b, int s_q, int h
   c.b = b;
   c.s_q = s_q;
   c.h_q = h_q;
+  c.num_parts = num_parts;
   return mla::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
                                                                                          : MLA_ERR_CUDA;
 }

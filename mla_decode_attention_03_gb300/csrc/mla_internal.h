@@ -54,6 +54,7 @@ struct CombineParams {
   void* out;
   float* lse;
   int b, s_q, h_q;
+  int num_parts;                 // the schedule's part count (host side: picks the kernel shape)
 };
 
 int decode_smem_bytes();

@@ -173,6 +173,47 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // out = 0 and lse = -inf.
 constexpr int kCombineWarps = 4;  // rows per block, one warp each
 
+// The common cut, a row in two pieces: both pieces' lse and values in one
+// round of loads, then merged (lane l takes columns [16l, 16l+16)).
+__device__ __forceinline__ void combine_two(const CombineParams& P, int rows, int row, int s0, int lane,
+                                            __nv_bfloat16* out, float* lse_out) {
+  const int64_t r0 = static_cast<int64_t>(s0) * rows + row, r1 = r0 + rows;
+  const float4* src0 = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r0 * kDimV) + lane * 4;
+  const float4* src1 = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r1 * kDimV) + lane * 4;
+  const float l0 = P.ws_lse[r0], l1 = P.ws_lse[r1];
+  float4 a[4], b[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    a[q] = src0[q];
+    b[q] = src1[q];
+  }
+  const float m = fmaxf(l0, l1);
+  float lse2 = -INFINITY, w0 = 0.f, w1 = 0.f;
+  if (m != -INFINITY) {
+    const float e0 = expf(l0 - m), e1 = expf(l1 - m);
+    const float inv = 1.f / (e0 + e1);
+    w0 = e0 * inv;
+    w1 = e1 * inv;
+    lse2 = m + logf(e0 + e1);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out) + lane * 2;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float4 x0 = a[2 * q], x1 = a[2 * q + 1], y0 = b[2 * q], y1 = b[2 * q + 1];
+    __nv_bfloat162 c0 = __floats2bfloat162_rn(w0 * x0.x + w1 * y0.x, w0 * x0.y + w1 * y0.y);
+    __nv_bfloat162 c1 = __floats2bfloat162_rn(w0 * x0.z + w1 * y0.z, w0 * x0.w + w1 * y0.w);
+    __nv_bfloat162 c2 = __floats2bfloat162_rn(w0 * x1.x + w1 * y1.x, w0 * x1.y + w1 * y1.y);
+    __nv_bfloat162 c3 = __floats2bfloat162_rn(w0 * x1.z + w1 * y1.z, w0 * x1.w + w1 * y1.w);
+    uint4 v;
+    v.x = *reinterpret_cast<uint32_t*>(&c0);
+    v.y = *reinterpret_cast<uint32_t*>(&c1);
+    v.z = *reinterpret_cast<uint32_t*>(&c2);
+    v.w = *reinterpret_cast<uint32_t*>(&c3);
+    dst[q] = v;
+  }
+  if (lane == 0) *lse_out = lse2;
+}
+
 __global__ void __launch_bounds__(32 * kCombineWarps) mla_combine_kernel(const CombineParams P) {
   grid_dependency_wait();  // the decode kernel's partials are complete and visible
   const int i = blockIdx.x;
@@ -188,43 +229,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) mla_combine_kernel(const C
   float* lse_out = P.lse + (static_cast<int64_t>(i) * P.h_q + h) * P.s_q + j;
 
   if (ns == 2) {
-    // The common cut (a sequence in two pieces): both pieces' lse and values
-    // are loaded in one round of loads, then merged.
-    const int64_t r0 = static_cast<int64_t>(s0) * rows + row, r1 = r0 + rows;
-    const float4* src0 = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r0 * kDimV) + lane * 4;
-    const float4* src1 = reinterpret_cast<const float4*>(static_cast<const float*>(P.ws_o) + r1 * kDimV) + lane * 4;
-    const float l0 = P.ws_lse[r0], l1 = P.ws_lse[r1];
-    float4 a[4], b[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      a[q] = src0[q];
-      b[q] = src1[q];
-    }
-    const float m = fmaxf(l0, l1);
-    float lse2 = -INFINITY, w0 = 0.f, w1 = 0.f;
-    if (m != -INFINITY) {
-      const float e0 = expf(l0 - m), e1 = expf(l1 - m);
-      const float inv = 1.f / (e0 + e1);
-      w0 = e0 * inv;
-      w1 = e1 * inv;
-      lse2 = m + logf(e0 + e1);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(out) + lane * 2;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float4 x0 = a[2 * q], x1 = a[2 * q + 1], y0 = b[2 * q], y1 = b[2 * q + 1];
-      __nv_bfloat162 c0 = __floats2bfloat162_rn(w0 * x0.x + w1 * y0.x, w0 * x0.y + w1 * y0.y);
-      __nv_bfloat162 c1 = __floats2bfloat162_rn(w0 * x0.z + w1 * y0.z, w0 * x0.w + w1 * y0.w);
-      __nv_bfloat162 c2 = __floats2bfloat162_rn(w0 * x1.x + w1 * y1.x, w0 * x1.y + w1 * y1.y);
-      __nv_bfloat162 c3 = __floats2bfloat162_rn(w0 * x1.z + w1 * y1.z, w0 * x1.w + w1 * y1.w);
-      uint4 v;
-      v.x = *reinterpret_cast<uint32_t*>(&c0);
-      v.y = *reinterpret_cast<uint32_t*>(&c1);
-      v.z = *reinterpret_cast<uint32_t*>(&c2);
-      v.w = *reinterpret_cast<uint32_t*>(&c3);
-      dst[q] = v;
-    }
-    if (lane == 0) *lse_out = lse2;
+    combine_two(P, rows, row, s0, lane, out, lse_out);
     return;
   }
 
@@ -275,6 +280,103 @@ __global__ void __launch_bounds__(32 * kCombineWarps) mla_combine_kernel(const C
   if (lane == 0) *lse_out = lse;
 }
 
+// The same merge when many pieces per sequence are expected (the schedule
+// has at least twice as many parts as sequences): four warps per row, each
+// taking every fourth piece of the row, so that four chains of loads are in
+// flight per row, their sums added through shared memory.  A block still
+// covers 4 rows of one sequence.
+constexpr int kCombineSplit = 4;  // warps per row
+
+__global__ void __launch_bounds__(32 * kCombineWarps * kCombineSplit, 1) mla_combine_many_kernel(const CombineParams P) {
+  __shared__ float4 red[kCombineSplit - 1][kCombineWarps][4][32];  // the other warps' sums, [q][lane] per row
+  grid_dependency_wait();  // the decode kernel's partials are complete and visible
+  const int i = blockIdx.x;
+  const int rows = P.s_q * P.h_q;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rw = warp % kCombineWarps;   // row within the block
+  const int part = warp / kCombineWarps;  // which of the row's warps
+  const int row = blockIdx.y * kCombineWarps + rw;
+  const bool live = row < rows;
+  const int s0 = P.num_splits[i];
+  const int ns = P.num_splits[i + 1] - s0;  // the same for the whole block
+  if (ns == 1) return;
+  const int j = row / P.h_q, h = row - (row / P.h_q) * P.h_q;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out) + (static_cast<int64_t>(i) * rows + row) * kDimV;
+  float* lse_out = P.lse + (static_cast<int64_t>(i) * P.h_q + h) * P.s_q + j;
+  const float* ws_o = static_cast<const float*>(P.ws_o);
+  if (ns == 2) {  // the same for the whole block: no barrier below is reached
+    if (part == 0 && live) combine_two(P, rows, row, s0, lane, out, lse_out);
+    return;
+  }
+
+  // every warp of a row forms the row's lse from all pieces' lse, then adds
+  // its own pieces' weighted values (no piece: out = 0, lse = -inf)
+  float4 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse = -INFINITY;
+  if (live && ns > 0) {
+    float mx = -INFINITY;
+    for (int k = lane; k < ns; k += 32) mx = fmaxf(mx, P.ws_lse[static_cast<int64_t>(s0 + k) * rows + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (mx != -INFINITY) {
+      float sum = 0.f;
+      for (int k = lane; k < ns; k += 32) sum += expf(P.ws_lse[static_cast<int64_t>(s0 + k) * rows + row] - mx);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      lse = mx + logf(sum);
+      for (int k = part; k < ns; k += kCombineSplit) {
+        const int64_t r = static_cast<int64_t>(s0 + k) * rows + row;
+        const float wgt = expf(P.ws_lse[r] - lse);
+        // lane l merges columns [16l, 16l+16): four 16-byte loads of fp32
+        const float4* src = reinterpret_cast<const float4*>(ws_o + r * kDimV) + lane * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = src[q];
+          acc[q].x += wgt * v.x;
+          acc[q].y += wgt * v.y;
+          acc[q].z += wgt * v.z;
+          acc[q].w += wgt * v.w;
+        }
+      }
+    }
+  }
+  if (part > 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) red[part - 1][rw][q][lane] = acc[q];
+  }
+  __syncthreads();
+  if (part != 0 || !live) return;
+#pragma unroll
+  for (int o = 0; o < kCombineSplit - 1; ++o) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = red[o][rw][q][lane];
+      acc[q].x += v.x;
+      acc[q].y += v.y;
+      acc[q].z += v.z;
+      acc[q].w += v.w;
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out) + lane * 2;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[2 * q].x, acc[2 * q].y);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q].z, acc[2 * q].w);
+    __nv_bfloat162 c = __floats2bfloat162_rn(acc[2 * q + 1].x, acc[2 * q + 1].y);
+    __nv_bfloat162 d = __floats2bfloat162_rn(acc[2 * q + 1].z, acc[2 * q + 1].w);
+    uint4 v;
+    v.x = *reinterpret_cast<uint32_t*>(&a);
+    v.y = *reinterpret_cast<uint32_t*>(&b2);
+    v.z = *reinterpret_cast<uint32_t*>(&c);
+    v.w = *reinterpret_cast<uint32_t*>(&d);
+    dst[q] = v;
+  }
+  if (lane == 0) *lse_out = lse;
+}
+
 }  // namespace
 
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, int32_t* metadata,
@@ -296,16 +398,20 @@ cudaError_t launch_metadata(const int32_t* cache_seqlens, int b, int num_parts, 
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   const int rows = p.s_q * p.h_q;
+  // Many pieces per sequence (at least twice as many parts as sequences, as
+  // with small batches on one CTA per SM): four warps per row.  Otherwise
+  // mostly one or two pieces: one warp per row, four rows per block.
+  const bool many = p.num_parts >= 2 * p.b;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.b, (rows + kCombineWarps - 1) / kCombineWarps, 1);
-  cfg.blockDim = dim3(32 * kCombineWarps, 1, 1);
+  cfg.blockDim = dim3(32 * kCombineWarps * (many ? kCombineSplit : 1), 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
+  return many ? cudaLaunchKernelEx(&cfg, mla_combine_many_kernel, p) : cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
 }
 
 }  // namespace mla
