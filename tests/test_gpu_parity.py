@@ -228,3 +228,44 @@ def test_num_parts_follows_the_kernel():
     assert ops.num_parts(2, 8, 1) == sms              # 2 positions x 8 heads = 16 rows
     assert ops.num_parts(2, 128, 1) == big // 2       # two 128-row tiles
     assert ops.num_parts(1, 32, 1) == big             # 32 rows: the cluster kernel
+
+
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_heads_identical_and_permuted(h_q):
+    """Two identical query heads give bit-identical outputs, and permuting the
+    heads permutes the outputs: bit for bit on the 16-row kernel (every row
+    takes the same steps); to the tolerance on the cluster kernel, whose
+    low-part pass is asked for by a warp of 16 rows for all of them, so a row
+    moved to another warp may take it where it did not before."""
+    w = W.make(3, 1, h_q, 1, [700, 77, 1500], stride=640, seed=41)
+    w.q[:, :, 3] = w.q[:, :, 1]
+    o, l, _, _ = run_gpu(w, parts=7)
+    assert torch.equal(o[:, :, 3], o[:, :, 1]) and torch.equal(l[:, 3], l[:, 1])
+    perm = torch.from_numpy(np.random.default_rng(6).permutation(h_q))
+    w2 = W.Workload(**{**w.__dict__, "q": w.q[:, :, perm].contiguous()})
+    o2, l2, _, _ = run_gpu(w2, parts=7)
+    po, pl = o[:, :, perm.to(o.device)], l[:, perm.to(l.device)]
+    if h_q <= 16:
+        assert torch.equal(o2, po) and torch.equal(l2, pl)
+    else:
+        ref = po.float()
+        assert torch.all((o2.float() - ref).abs() <= 1e-2 + 2e-2 * ref.abs())
+        assert torch.all((l2 - pl).abs() <= 1e-3)
+
+
+@pytest.mark.parametrize("h_q", [128, 8])
+def test_causal_positions_equal_shorter_noncausal_runs(h_q):
+    """With causal and s_q = 2, query 1 sees all L tokens and query 0 the
+    first L - 1: each equals a non-causal s_q = 1 decode of that length (to
+    the tolerance: the two runs take different schedules)."""
+    L = [300, 65, 1000]
+    w = W.make(3, 2, h_q, 1, L, stride=576, causal=True, seed=42)
+    o, l, _, _ = run_gpu(w)
+    for j in (0, 1):
+        lens = torch.tensor([x - 1 + j for x in L], dtype=torch.int32)
+        w1 = W.Workload(**{**w.__dict__, "q": w.q[:, j:j + 1].contiguous(), "s_q": 1, "causal": False,
+                           "cache_seqlens": lens})
+        o1, l1, _, _ = run_gpu(w1)
+        ref = o1[:, 0].float()
+        assert torch.all((o[:, j].float() - ref).abs() <= 1e-2 + 2e-2 * ref.abs())
+        assert torch.all((l[:, :, j] - l1[:, :, 0]).abs() <= 1e-3)
