@@ -521,14 +521,15 @@ def run_reference(args, world, rank):
 
 def run_sweep(args):
     """Bandwidth against mean sequence length at b=128, h_q=128 (the shape of the
-    seqlen sweep plotted in the PAI tutorial, section 4), for the 576- and
+    seqlen sweep plotted in the PAI tutorial, section 4; `--sweep-heads` sets
+    another head count, e.g. 16 for the 16-row kernel), for the 576- and
     640-element entry layouts.  Inputs are drawn on the device (a seeded
     torch generator): this mode times only, it compares nothing."""
     from mla_decode_attention_03_gb300 import ops
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    b, h_q = 128, 128
+    b, h_q = 128, args.sweep_heads
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -684,6 +685,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", default=None,
                     help="comma-separated mean sequence lengths: print one line per (length, stride)")
+    ap.add_argument("--sweep-heads", type=int, default=128, help="query heads (h_kv = 1) of the --sweep batch")
     ap.add_argument("--cache-ops", action="store_true",
                     help="time the cache write and copy_blocks kernels instead of the decode step")
     ap.add_argument("--e2e-runs", default=None,
