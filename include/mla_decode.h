@@ -154,6 +154,8 @@ mla_status_t mla_decode_with_kvcache(const void *q, int b, int s_q, int h_q, int
  * Flash-Decoding merge) into out and lse, and writes out = 0, lse = -inf for
  * sequences of length 0.  It must run after mla_decode_splitkv on the same
  * workspace, b, s_q, h_q and num_parts; ordering on one stream suffices.
+ * num_parts also sets the merge kernel's shape: with num_parts >= 2 b
+ * (sequences in many pieces) each row gets four warps, otherwise one.
  *
  * Both kernels are launched with programmatic dependent launch: they may
  * start their set-up (shared and tensor memory only) while the kernel before
