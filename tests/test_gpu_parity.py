@@ -14,7 +14,7 @@ import torch
 
 from mla_decode_attention_03_gb300 import ops
 from mla_decode_attention_03_gb300 import workloads as W
-from tests._gpu_helpers import all_rows, assert_matches, run_gpu, to_device
+from tests._gpu_helpers import all_rows, assert_matches, run_gpu, sample_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -269,3 +269,17 @@ def test_causal_positions_equal_shorter_noncausal_runs(h_q):
         ref = o1[:, 0].float()
         assert torch.all((o[:, j].float() - ref).abs() <= 1e-2 + 2e-2 * ref.abs())
         assert torch.all((l[:, :, j] - l1[:, :, 0]).abs() <= 1e-3)
+
+
+@pytest.mark.parametrize("h_q", KERNEL_HEADS)
+def test_thousands_of_short_sequences_sampled(h_q):
+    """4096 sequences of 1-200 tokens: every part walks tens of segments (Q
+    buffers, epilogues, split slots turn over many times); 3000 sampled rows
+    plus the first and last sequence's rows against the oracle."""
+    b = 4096
+    sl = list(np.random.default_rng(4).integers(1, 200, size=b))
+    w = W.make(b, 1, h_q, 1, sl, stride=640, seed=43, poison=True)
+    out, lse, _, nsplit = run_gpu(w)
+    assert int(nsplit[-1].item()) > b  # some sequences are cut
+    extra = [(i, 0, h) for i in (0, b - 1) for h in range(h_q)]
+    assert_matches(w, out, lse, sample_rows(w, 3000, seed=5, extra=extra))
